@@ -1,0 +1,129 @@
+/*
+ * lp_ragged.h — C ABI of the GB300 ragged batched log-probability library.
+ *
+ * The operation (from "MAX Python SDK 中 log_probabilities 模块解析", sections
+ * "两个核心函数的 API 契约", "ragged 数据编排：从输入缓冲到 kernel 调用" and
+ * "top-k 语义：堆式 kernel 与「采样 token 兜底」"; the logprob definition from
+ * "logprob、finish reason 与 output processing", section "logprob 的数值形态"):
+ *
+ *   batch b owns logits rows [off[b], off[b+1]) of an fp32 [T, V] matrix;
+ *   it emits len_b output rows when echo[b] is set, else one row (its last
+ *   position); output_row_offsets = [0, cumsum(counts)], R = output_row_offsets[B].
+ *   For every output row o scoring logits row r:
+ *     lse            = log(sum_v exp(x[r, v]))
+ *     columns 0..K-1 = the K = 2^levels - 1 best tokens of the row under
+ *                      (logit descending, token id ascending), as
+ *                      (x[r, id] - lse, id), padded with (-inf, 0xFFFFFFFF)
+ *                      when V < K;
+ *     column K       = (x[r, t] - lse, t), t = tokens[r+1] when r+1 is still in
+ *                      the sequence, else sampled_tokens[b].
+ *   W = out_per_token = 2^levels (1 when levels == 0) columns per row.
+ *
+ * Conventions shared by every entry point
+ *   - Ownership: the caller owns every buffer (device memory, the workspace, the
+ *     host words) and the stream. The library allocates nothing, keeps no state
+ *     between calls apart from a per-device launch-shape cache, and may be called
+ *     from several host threads on different workspaces.
+ *   - Asynchrony: all device work is enqueued on `stream`; a return of LP_OK means
+ *     "validated and enqueued", not "finished".
+ *   - Host-checked errors are returned at once and nothing is enqueued.
+ *   - Device-detected errors never trap: they set bits in the workspace status
+ *     word (bit c set <=> error code c seen), read with lp_ragged_read_status.
+ *   - Integers are uint32; echo flags are one byte each (0 = off).
+ *   - Logits must be finite or -inf. -inf tokens have probability 0; a row of only
+ *     -inf yields NaN logprobs. NaN or +inf logits give unspecified values (no fault).
+ */
+#ifndef LP_RAGGED_H
+#define LP_RAGGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; 0 is the legacy default stream. */
+typedef struct CUstream_st *lp_stream_t;
+
+typedef enum lp_status {
+    LP_OK = 0,
+    LP_ERR_NULL = 1,         /* a required pointer is NULL                                  */
+    LP_ERR_LEVELS = 2,       /* levels > LP_MAX_LEVELS                                      */
+    LP_ERR_SHAPE = 3,        /* B, T or V is 0 or too large, or logits not 4-byte aligned   */
+    LP_ERR_OFFSETS = 4,      /* device: empty or decreasing batch range, a range past T, or
+                                output offsets that disagree with the echo flags           */
+    LP_ERR_TOKEN_RANGE = 5,  /* device: an actual or sampled token >= V                     */
+    LP_ERR_WORKSPACE = 6,    /* workspace NULL or smaller than lp_ragged_workspace_size     */
+    LP_ERR_CUDA = 7          /* a CUDA launch or copy failed                                */
+} lp_status;
+
+#define LP_MAX_LEVELS 6u
+#define LP_PAD_TOKEN 0xFFFFFFFFu
+
+/*
+ * Bytes of scratch the two calls need on the CURRENT device (it depends on the
+ * device's SM count and on levels only; B, T and V are accepted for forward
+ * compatibility). Returns 0 when levels > LP_MAX_LEVELS or no device is usable.
+ * The workspace holds the status word, per-CTA arrival counters and the split-row
+ * partial tuples (max, sum-exp, top-K). One workspace per concurrently running call.
+ */
+size_t lp_ragged_workspace_size(uint32_t B, uint32_t T, uint32_t V, uint32_t levels);
+
+/*
+ * Step 1 — output-row plan (MAX page, "ragged 数据编排"): one device prefix sum of
+ * count_b = echo[b] ? len_b : 1.
+ *   logit_row_offsets   device, uint32[B+1], the input row offsets (next-token
+ *                       logits: 0..B)
+ *   echo                device, uint8[B]
+ *   B, T                batches, logits rows
+ *   output_row_offsets  device out, uint32[B+1]
+ *   host_rows_and_status  optional host out (pinned for a truly async copy), two
+ *                       words {R, status bits}; valid after the stream reaches this
+ *                       point. Pass NULL to skip the copy.
+ *   workspace           device, >= lp_ragged_workspace_size bytes; plan clears its
+ *                       status word and arrival counters, so call plan before the
+ *                       first compute on a workspace.
+ * Device checks: len_b >= 1, off[b+1] <= T  (LP_ERR_OFFSETS bit).
+ */
+lp_status lp_ragged_plan(const uint32_t *logit_row_offsets, const uint8_t *echo, uint32_t B, uint32_t T,
+                         uint32_t *output_row_offsets, uint32_t *host_rows_and_status,
+                         void *workspace, size_t workspace_bytes, lp_stream_t stream);
+
+/*
+ * Step 2 — the streaming reduction (MAX page, "top-k 语义：堆式 kernel 与「采样
+ * token 兜底」"): one pass over each scored logits row computing the online max and
+ * sum-exp, the top-K under (logit desc, id asc), and the target token's logit.
+ *   logits              device, float[T][V] row-major (any 4-byte alignment)
+ *   logit_row_offsets   device, uint32[B+1]
+ *   tokens              device, uint32[T], flat input tokens
+ *   sampled_tokens      device, uint32[B]
+ *   output_row_offsets  device, uint32[B+1], as written by lp_ragged_plan
+ *   echo                device, uint8[B]
+ *   levels              0..LP_MAX_LEVELS; K = 2^levels - 1, W = 2^levels (1 if 0)
+ *   out_logprobs        device out, float[R][W]
+ *   out_tokens          device out, uint32[R][W]
+ *   R = output_row_offsets[B] is read on the device; the outputs must hold R*W
+ *   entries each. Rows are split across CTAs when R is small (decode); the CTA that
+ *   finishes a row's last piece merges the pieces, so there is a single launch.
+ * Device checks: the offsets checks of plan (a bad batch is skipped), and
+ *   tokens/sampled < V (LP_ERR_TOKEN_RANGE; that row's column K gets logprob NaN).
+ */
+lp_status lp_ragged_compute(const float *logits, uint32_t T, uint32_t V,
+                            const uint32_t *logit_row_offsets, uint32_t B,
+                            const uint32_t *tokens, const uint32_t *sampled_tokens,
+                            const uint32_t *output_row_offsets, const uint8_t *echo, uint32_t levels,
+                            float *out_logprobs, uint32_t *out_tokens,
+                            void *workspace, size_t workspace_bytes, lp_stream_t stream);
+
+/* Enqueue a copy of the workspace status word (bit c <=> lp_status c) to host. */
+lp_status lp_ragged_read_status(const void *workspace, uint32_t *host_status, lp_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *lp_ragged_strerror(lp_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LP_RAGGED_H */

@@ -1,0 +1,211 @@
+"""Plain fp64 CPU oracle for ragged batched log-probabilities.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, ``__graft_entry__.smoke()``
+and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or
+run this module.  It shares no code with the CUDA path (``ragged_log_probs_gb300``)
+and imports nothing from it.
+
+What it computes (the plain definition, written out, slow on purpose):
+
+* Output layout — "MAX Python SDK 中 log_probabilities 模块解析", section
+  "ragged 数据编排：从输入缓冲到 kernel 调用": batch ``b`` owns logits rows
+  ``[off[b], off[b+1])``; it emits ``len_b`` output rows when echo is on and one
+  row otherwise; the output offsets are ``[0]`` followed by the running sum of
+  those counts.
+* Columns — same page, sections "两个核心函数的 API 契约" and "top-k 语义：堆式
+  kernel 与「采样 token 兜底」": ``out_per_token = 2**levels`` (1 when
+  ``levels == 0``); the first ``2**levels - 1`` columns hold the top candidates,
+  the last column holds the actual (for the last position: sampled) token.
+* Value — "logprob、finish reason 与 output processing", section "logprob 的数值
+  形态": a logprob is the natural log of the softmax probability, ``x_v - lse``.
+* Which token a row scores — same SGLang page, section "input logprob 和 output
+  logprob 来自哪里": a prompt position scores the next prompt token; the decode
+  step scores the sampled token.
+
+Readings taken where the pages are silent (each is also listed in the design doc):
+
+* Non-echo batches read the LAST logits row of their sequence (for next-token
+  logits with ``off = arange(B+1)`` that row is the only one).
+* Top-k order: fp32 logit descending, ties by ascending token id; padding columns
+  (vocab smaller than k) carry id ``0xFFFFFFFF`` and logprob ``-inf``.
+* ``-inf`` logits are valid tokens with probability 0; a row of only ``-inf``
+  has ``lse = NaN`` semantics (``-inf - -inf``), so all its logprobs are NaN.
+* A target token ``>= V`` gets logprob NaN and is reported as an error.
+* Raw logits, no temperature.
+
+Every function here has a pin in ``tests/test_oracle_pins.py``.
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Callable, Sequence, Union
+
+import numpy as np
+
+PAD_ID = 0xFFFFFFFF
+
+RowSource = Union[np.ndarray, Callable[[int], np.ndarray]]
+
+
+def out_per_token(levels: int) -> int:
+    """Columns per output row: ``2**levels``, or 1 when ``levels == 0``.
+
+    "MAX Python SDK 中 log_probabilities 模块解析", section "两个核心函数的 API 契约".
+    """
+    if levels < 0:
+        raise ValueError("levels must be >= 0")
+    return 2 ** levels if levels > 0 else 1
+
+
+def top_k_capacity(levels: int) -> int:
+    """Largest top-n a graph built with ``levels`` can return: ``2**levels - 1``.
+
+    Same page, section "图支持的最大 top-n" (``levels=3`` gives 7); the extra
+    column of ``out_per_token`` is reserved for the sampled token.
+    """
+    return out_per_token(levels) - 1
+
+
+def levels_for_top_n(top_n: int) -> int:
+    """Smallest ``levels`` whose capacity ``2**levels - 1`` covers ``top_n``.
+
+    Same page, section "两个核心函数的 API 契约": ``logprobs=5`` needs ``levels=3``.
+    """
+    if top_n < 0:
+        raise ValueError("top_n must be >= 0")
+    levels = 0
+    while 2 ** levels - 1 < top_n:
+        levels += 1
+    return levels
+
+
+def validate_offsets(logit_row_offsets: Sequence[int], T: int) -> None:
+    """Offsets must be non-empty per batch and stay inside the ``T`` logits rows.
+
+    Batch ``n`` owns rows ``[off[n], off[n+1])`` (same page, section "两个核心函数
+    的 API 契约"); an empty range is rejected because a non-echo batch would then
+    read another batch's row.
+    """
+    off = [int(v) for v in logit_row_offsets]
+    if len(off) < 2:
+        raise ValueError("need at least one batch")
+    for b in range(len(off) - 1):
+        if off[b + 1] <= off[b]:
+            raise ValueError(f"batch {b} has an empty or decreasing row range")
+    if off[-1] > T:
+        raise ValueError("offsets run past the logits rows")
+
+
+def output_row_offsets(logit_row_offsets: Sequence[int], echo: Sequence[bool]) -> np.ndarray:
+    """``[0] ++ cumsum(count_b)``, ``count_b = len_b`` if echo else 1.
+
+    Same page, section "ragged 数据编排：从输入缓冲到 kernel 调用".
+    """
+    off = [int(v) for v in logit_row_offsets]
+    B = len(off) - 1
+    if len(echo) != B:
+        raise ValueError("echo must have one flag per batch")
+    out = [0]
+    for b in range(B):
+        count = (off[b + 1] - off[b]) if bool(echo[b]) else 1
+        out.append(out[-1] + count)
+    return np.asarray(out, dtype=np.uint64)
+
+
+def output_rows(logit_row_offsets: Sequence[int], echo: Sequence[bool],
+                tokens: Sequence[int], sampled_tokens: Sequence[int]) -> list[tuple[int, int, int]]:
+    """For every output row in order: ``(batch, logits_row, target_token)``.
+
+    Echo batches emit one row per input position, non-echo batches one row for
+    their last position; the row of position ``i`` scores token ``i + 1`` of the
+    same sequence, and the last position scores the batch's sampled token.
+    ("input logprob 和 output logprob 来自哪里" on the SGLang page; sampled-token
+    slot in "compute_top 的结果组装" on the MAX page.)
+    """
+    off = [int(v) for v in logit_row_offsets]
+    rows = []
+    for b in range(len(off) - 1):
+        start, end = off[b], off[b + 1]
+        count = (end - start) if bool(echo[b]) else 1
+        for j in range(count):
+            r = end - count + j
+            t = int(tokens[r + 1]) if r + 1 < end else int(sampled_tokens[b])
+            rows.append((b, r, t))
+    return rows
+
+
+def row_logsumexp(x32: np.ndarray) -> float:
+    """``log(sum(exp(x)))`` of one fp32 row, evaluated in fp64 with the max shift."""
+    x = np.asarray(x32, dtype=np.float64)
+    m = x.max()
+    return float(m + np.log(np.sum(np.exp(x - m))))
+
+
+def row_top_k_ids(x32: np.ndarray, k: int) -> np.ndarray:
+    """The ``k`` best ids of a row under (fp32 logit desc, id asc), padded with PAD_ID.
+
+    A full stable sort of the whole row — no selection tricks.
+    """
+    x = np.asarray(x32, dtype=np.float32)
+    ids = np.arange(x.shape[0], dtype=np.int64)
+    order = np.lexsort((ids, -x.astype(np.float64)))  # primary: -x ascending; secondary: id ascending
+    top = order[:k].astype(np.uint64)
+    if top.shape[0] < k:
+        top = np.concatenate([top, np.full(k - top.shape[0], PAD_ID, dtype=np.uint64)])
+    return top
+
+
+def _get_row(logits: RowSource, r: int) -> np.ndarray:
+    if callable(logits):
+        return np.asarray(logits(r), dtype=np.float32)
+    return np.asarray(logits[r], dtype=np.float32)
+
+
+def score_row(x32: np.ndarray, target: int, levels: int) -> tuple[np.ndarray, np.ndarray, bool]:
+    """One output row: ``W`` logprobs (fp64) and ids; flag says the target was in range."""
+    V = x32.shape[0]
+    K = top_k_capacity(levels)
+    W = out_per_token(levels)
+    x = np.asarray(x32, dtype=np.float64)
+    lse = row_logsumexp(x32)
+    lp = np.empty(W, dtype=np.float64)
+    tok = np.empty(W, dtype=np.uint64)
+    if K > 0:
+        top = row_top_k_ids(x32, K)
+        for c in range(K):
+            tok[c] = top[c]
+            lp[c] = (x[int(top[c])] - lse) if top[c] != PAD_ID else -math.inf
+    in_range = 0 <= target < V
+    tok[K] = target
+    lp[K] = (x[target] - lse) if in_range else math.nan
+    return lp, tok, in_range
+
+
+def ragged_log_probs(logits: RowSource, logit_row_offsets: Sequence[int], tokens: Sequence[int],
+                     sampled_tokens: Sequence[int], echo: Sequence[bool], levels: int,
+                     rows: Sequence[int] | None = None, T: int | None = None):
+    """Reference result of the whole path.
+
+    ``logits`` is a 2-D fp32 array ``[T, V]`` or a callable ``r -> row``.
+    Returns ``(out_offsets u64[B+1], logprobs f64[R', W], token_ids u64[R', W],
+    all_targets_in_range)`` where ``R'`` is every output row, or only ``rows``
+    (output-row indices) when given.
+    """
+    if T is None:
+        T = int(logits.shape[0]) if not callable(logits) else int(logit_row_offsets[-1])
+    validate_offsets(logit_row_offsets, T)
+    if levels < 0:
+        raise ValueError("levels must be >= 0")
+    out_off = output_row_offsets(logit_row_offsets, echo)
+    mapping = output_rows(logit_row_offsets, echo, tokens, sampled_tokens)
+    wanted = range(len(mapping)) if rows is None else [int(o) for o in rows]
+    W = out_per_token(levels)
+    lp = np.empty((len(wanted), W), dtype=np.float64)
+    tok = np.empty((len(wanted), W), dtype=np.uint64)
+    ok = True
+    for i, o in enumerate(wanted):
+        _, r, t = mapping[o]
+        lp[i], tok[i], in_range = score_row(_get_row(logits, r), t, levels)
+        ok = ok and in_range
+    return out_off, lp, tok, ok

@@ -1,0 +1,101 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins catch
+each one: a pin set that lets a wrong oracle pass proves nothing."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.ragged_oracle as ro
+from tests import test_oracle_pins as pins
+
+PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
+
+
+def _lse_without_log(x32):
+    x = np.asarray(x32, dtype=np.float64)
+    m = x.max()
+    return float(m + np.sum(np.exp(x - m)))
+
+
+def _lse_without_shift_back(x32):
+    x = np.asarray(x32, dtype=np.float64)
+    m = x.max()
+    return float(np.log(np.sum(np.exp(x - m))))
+
+
+def _top_k_ties_reversed(x32, k):
+    x = np.asarray(x32, dtype=np.float32)
+    ids = np.arange(x.shape[0])
+    order = np.lexsort((-ids, -x.astype(np.float64)))
+    top = order[:k].astype(np.uint64)
+    if top.shape[0] < k:
+        top = np.concatenate([top, np.full(k - top.shape[0], oracle.PAD_ID, dtype=np.uint64)])
+    return top
+
+
+def _rows_target_same_position(off, echo, tokens, sampled):
+    rows = []
+    for b in range(len(off) - 1):
+        s, e = int(off[b]), int(off[b + 1])
+        cnt = (e - s) if echo[b] else 1
+        for j in range(cnt):
+            r = e - cnt + j
+            rows.append((b, r, int(tokens[r]) if r + 1 < e else int(sampled[b])))
+    return rows
+
+
+def _rows_first_position(off, echo, tokens, sampled):
+    rows = []
+    for b in range(len(off) - 1):
+        s, e = int(off[b]), int(off[b + 1])
+        cnt = (e - s) if echo[b] else 1
+        for j in range(cnt):
+            r = s + j
+            rows.append((b, r, int(tokens[r + 1]) if r + 1 < e else int(sampled[b])))
+    return rows
+
+
+def _offsets_short_count(off, echo):
+    out = [0]
+    for b in range(len(off) - 1):
+        out.append(out[-1] + ((int(off[b + 1]) - int(off[b]) - 1) if echo[b] else 1))
+    return np.asarray(out, dtype=np.uint64)
+
+
+def _score_row_sign_flipped(x32, target, levels):
+    lp, tok, ok = _orig_score_row(x32, target, levels)
+    return -lp, tok, ok
+
+
+def _out_per_token_no_slot(levels):
+    return 2 ** levels - 1 if levels > 0 else 1
+
+
+_orig_score_row = ro.score_row
+
+MUTATIONS = {
+    "lse_drops_log": ("row_logsumexp", _lse_without_log),
+    "lse_drops_max": ("row_logsumexp", _lse_without_shift_back),
+    "ties_by_higher_id": ("row_top_k_ids", _top_k_ties_reversed),
+    "target_off_by_one": ("output_rows", _rows_target_same_position),
+    "non_echo_reads_first_row": ("output_rows", _rows_first_position),
+    "echo_count_short": ("output_row_offsets", _offsets_short_count),
+    "logprob_sign_flipped": ("score_row", _score_row_sign_flipped),
+    "no_sampled_slot": ("out_per_token", _out_per_token_no_slot),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(ro, attr, fn)
+    monkeypatch.setattr(oracle, attr, fn, raising=False)
+    failures = 0
+    for t in PIN_TESTS:
+        try:
+            t()
+        except (AssertionError, ValueError, IndexError, TypeError):
+            failures += 1
+    assert failures > 0, f"no pin caught the planted mistake {name!r}"

@@ -1,0 +1,244 @@
+"""Pins that tie the fp64 oracle to what the pages and the mathematics fix.
+
+None of these re-type the oracle's formulas: they use values printed on the pages,
+closed forms (dyadic distributions, uniform rows), an independent library routine
+(scipy's log_softmax), and brute force by pairwise counting on tiny rows.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from oracle import PAD_ID
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --- worked constants (MAX page: API contract, max top-n) -------------------------
+
+def test_levels_worked_values():
+    g = _golden("page_constants.json")
+    for top_n, levels in g["levels_examples"]["top_n_to_levels"]:
+        assert oracle.levels_for_top_n(top_n) == levels
+    for levels, w in g["levels_examples"]["levels_to_out_per_token"]:
+        assert oracle.out_per_token(levels) == w
+    assert oracle.top_k_capacity(g["max_top_n"]["levels"]) == g["max_top_n"]["max_top_n"]
+
+
+def test_levels_relation_all():
+    for levels in range(0, 7):
+        k = oracle.top_k_capacity(levels)
+        assert oracle.out_per_token(levels) == k + 1
+        assert oracle.levels_for_top_n(k) == levels
+        if levels:
+            assert oracle.levels_for_top_n(k + 1) == levels + 1
+    assert oracle.top_k_capacity(6) == 63
+    with pytest.raises(ValueError):
+        oracle.levels_for_top_n(-1)
+
+
+# --- layout (MAX page: ragged data layout) ----------------------------------------
+
+def test_tiny_layout_golden():
+    g = _golden("tiny_layout.json")
+    off = np.concatenate([[0], np.cumsum(g["lengths"])])
+    got = oracle.output_row_offsets(off, g["echo"])
+    assert got.tolist() == g["output_row_offsets"]
+    assert np.diff(got).tolist() == g["output_counts"]
+    rows = oracle.output_rows(off, g["echo"], tokens=np.zeros(off[-1], int), sampled_tokens=[0] * 4)
+    assert [r for (_, r, _) in rows] == g["logit_rows_scored"]
+
+
+def test_next_token_layout_is_arange():
+    B = 9
+    off = np.arange(B + 1)
+    got = oracle.output_row_offsets(off, [False] * B)
+    assert got.tolist() == list(range(B + 1))
+    rows = oracle.output_rows(off, [False] * B, tokens=np.arange(B), sampled_tokens=np.arange(100, 100 + B))
+    assert [(b, r, t) for (b, r, t) in rows] == [(b, b, 100 + b) for b in range(B)]
+
+
+def test_target_is_next_input_token_then_sampled():
+    # SGLang page, "input logprob 和 output logprob 来自哪里": a prompt position
+    # scores the following prompt token; the final position scores the sampled one.
+    off = [0, 3, 5]
+    tokens = [10, 11, 12, 20, 21]
+    rows = oracle.output_rows(off, [True, False], tokens, [99, 98])
+    assert rows == [(0, 0, 11), (0, 1, 12), (0, 2, 99), (1, 4, 98)]
+    rows = oracle.output_rows(off, [False, True], tokens, [99, 98])
+    assert rows == [(0, 2, 99), (1, 3, 21), (1, 4, 98)]
+
+
+def test_invalid_offsets_rejected():
+    with pytest.raises(ValueError):
+        oracle.validate_offsets([0, 2, 2, 5], 5)      # empty batch
+    with pytest.raises(ValueError):
+        oracle.validate_offsets([0, 3, 2], 5)         # decreasing
+    with pytest.raises(ValueError):
+        oracle.validate_offsets([0, 3, 7], 5)         # past T
+    oracle.validate_offsets([0, 3, 5], 5)
+
+
+# --- values (SGLang page: logprob numeric form) -----------------------------------
+
+def test_dyadic_row_closed_form_and_tie_order():
+    p = np.array([0.5, 0.25, 0.125, 0.125])
+    x = np.log(p).astype(np.float32)
+    lp, tok, ok = oracle.score_row(x, target=3, levels=2)
+    assert ok
+    assert tok.tolist() == [0, 1, 2, 3]        # ids 2 and 3 tie: lower id first
+    np.testing.assert_allclose(lp, np.log(p[[0, 1, 2, 3]]), atol=1e-7)
+    # fp32 logits of exact powers of two: ln(2^-k) rounded to fp32 differs from the
+    # fp64 value by < 1e-7; the dyadic sum itself is exact.
+
+
+def test_page_probability_examples():
+    g = _golden("page_constants.json")["probability_examples"]
+    for lp_print, pct in g["logprob_to_percent"]:
+        assert round(100 * math.exp(lp_print)) == pct
+    # A three-token distribution with those probabilities, shifted by an arbitrary
+    # constant (softmax is shift-invariant): natural-log logprobs come back.
+    probs = np.array([0.154, 0.122, 0.724])
+    x = (np.log(probs) + 7.5).astype(np.float32)
+    lp, tok, _ = oracle.score_row(x, target=0, levels=2)
+    assert tok[:3].tolist() == [2, 0, 1]
+    assert round(lp[1], 2) == -1.87 and round(lp[2], 2) == -2.10
+    assert round(lp[3], 2) == -1.87
+
+
+def test_uniform_row_is_minus_log_v():
+    V = 1000
+    x = np.full(V, 3.25, dtype=np.float32)
+    lp, tok, _ = oracle.score_row(x, target=17, levels=3)
+    assert tok[:7].tolist() == list(range(7))
+    np.testing.assert_allclose(lp, -math.log(V), atol=1e-12, rtol=0)
+
+
+def test_full_vocab_columns_sum_to_one():
+    rng = np.random.default_rng(5)
+    for V in (1, 2, 5, 7):
+        x = (rng.standard_normal(V) * 4).astype(np.float32)
+        lp, tok, _ = oracle.score_row(x, target=0, levels=3)
+        real = lp[:V]
+        assert abs(scipy.special.logsumexp(real)) < 1e-12
+        assert sorted(tok[:V].tolist()) == list(range(V))
+        assert all(t == PAD_ID for t in tok[V:7])
+        assert all(v == -math.inf for v in lp[V:7])
+
+
+def test_matches_scipy_log_softmax():
+    rng = np.random.default_rng(6)
+    for V in (3, 40, 63):
+        x = (rng.standard_normal(V) * 3).astype(np.float32)
+        ref = scipy.special.log_softmax(x.astype(np.float64))
+        for target in (0, V - 1):
+            lp, tok, _ = oracle.score_row(x, target=target, levels=6)
+            for c in range(min(V, 63)):
+                assert abs(lp[c] - ref[int(tok[c])]) < 1e-12
+            assert abs(lp[63] - ref[target]) < 1e-12
+
+
+def test_brute_force_rank_and_pairwise_values():
+    """Tiny rows with many exact ties, every levels: ids by pairwise rank counting,
+    values by lp_i = -log(sum_j exp(x_j - x_i)) summed with math.fsum."""
+    rng = np.random.default_rng(7)
+    for trial in range(40):
+        V = int(rng.integers(1, 65))
+        x = (np.round(rng.standard_normal(V) * 4) / 4).astype(np.float32)
+        if trial % 5 == 0:
+            x[rng.integers(0, V, size=max(1, V // 4))] = -np.inf
+        if np.all(np.isneginf(x)):
+            x[0] = 0.0
+        better = lambda j, i: (x[j] > x[i]) or (x[j] == x[i] and j < i)
+        rank = [sum(better(j, i) for j in range(V)) for i in range(V)]
+        by_rank = [None] * V
+        for i, r in enumerate(rank):
+            by_rank[r] = i
+        xs = [float(v) for v in x]
+        def brute_lp(i):
+            if xs[i] == -math.inf:
+                return -math.inf
+            return -math.log(math.fsum(math.exp(xj - xs[i]) for xj in xs if xj != -math.inf))
+        for levels in range(0, 7):
+            K = oracle.top_k_capacity(levels)
+            t = int(rng.integers(0, V))
+            lp, tok, ok = oracle.score_row(x, target=t, levels=levels)
+            assert ok and tok[K] == t
+            assert abs(lp[K] - brute_lp(t)) < 1e-9 or (lp[K] == brute_lp(t) == -math.inf)
+            for c in range(K):
+                if c < V:
+                    assert tok[c] == by_rank[c]
+                    want = brute_lp(by_rank[c])
+                    assert (lp[c] == want == -math.inf) or abs(lp[c] - want) < 1e-9
+                else:
+                    assert tok[c] == PAD_ID and lp[c] == -math.inf
+
+
+def test_lexsort_cross_check_large_row():
+    rng = np.random.default_rng(8)
+    V = 5000
+    x = (np.round(rng.standard_normal(V) * 16) / 16).astype(np.float32)
+    top = oracle.row_top_k_ids(x, 63)
+    # independent: python's sort on (-x, id) tuples
+    want = sorted(range(V), key=lambda i: (-float(x[i]), i))[:63]
+    assert top.tolist() == want
+
+
+# --- special values and invariants -------------------------------------------------
+
+def test_neg_inf_entries_rank_last():
+    x = np.array([-np.inf, 1.0, -np.inf, 0.5, -np.inf], dtype=np.float32)
+    lp, tok, _ = oracle.score_row(x, target=2, levels=3)
+    assert tok[:5].tolist() == [1, 3, 0, 2, 4]
+    assert lp[2] == -np.inf and lp[3] == -np.inf and lp[4] == -np.inf
+    assert lp[7] == -np.inf and tok[7] == 2
+    assert abs(np.logaddexp(lp[0], lp[1])) < 1e-12
+
+
+def test_all_neg_inf_row_is_nan_by_reading():
+    x = np.full(10, -np.inf, dtype=np.float32)
+    lp, tok, _ = oracle.score_row(x, target=4, levels=2)
+    assert tok.tolist() == [0, 1, 2, 4]
+    assert np.all(np.isnan(lp))
+
+
+def test_target_out_of_range_flags_nan():
+    x = np.zeros(8, dtype=np.float32)
+    lp, tok, ok = oracle.score_row(x, target=8, levels=1)
+    assert not ok and tok[1] == 8 and math.isnan(lp[1])
+
+
+def test_invariants_on_tiny_workload():
+    import workloads
+    b = workloads.make_batch("tiny", "cpu")
+    off, tok_in, sampled, echo = b.host()
+    out_off, lp, tok, ok = oracle.ragged_log_probs(b.logits.numpy(), off, tok_in, sampled, echo, b.levels)
+    assert ok
+    assert out_off.tolist() == _golden("tiny_layout.json")["output_row_offsets"]
+    assert lp.shape == (6, 8)
+    assert np.all(lp <= 0)
+    x = b.logits.numpy()
+    rows = oracle.output_rows(off, echo, tok_in, sampled)
+    for o, (_, r, t) in enumerate(rows):
+        # top-k is sorted: non-increasing logit, ascending id within a tie
+        keys = [(-float(x[r, i]), int(i)) for i in tok[o, :7]]
+        assert keys == sorted(keys)
+        # the actual-token column equals the top-k entry when the id coincides
+        for c in range(7):
+            if tok[o, c] == t:
+                assert lp[o, c] == lp[o, 7]
+    # row 0 of the tiny workload holds two exactly tied maxima, lower id first
+    r0 = x[0]
+    ties = np.flatnonzero(r0 == r0.max())
+    assert len(ties) == 2
+    assert tok[0, :2].tolist() == sorted(ties.tolist())
