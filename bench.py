@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Benchmark of the ragged batched log-probability path on GB300.
+
+One step = the whole hot path over one synthetic batch: ``lp_ragged_plan`` (output
+offsets) + ``lp_ragged_compute`` (streaming max / sum-exp / top-k / target gather,
+split-row merge). Default workload: decode, B=256 next-token rows of V=128256,
+levels=3, no echo. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle (the only reference that exists for
+this path) on the host cores, on the same workload, one bounded sample per step.
+Under torchrun every rank runs its own batch (weak scaling, no collective on the
+data path); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "logit rows/sec and achieved HBM GB/s (fraction of GB300 peak) for ragged logprobs+top-k"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_TEXT = {
+    "tiny": "tiny: B=4, lengths {3,5,1,7}, V=1000, levels=3, echo {T,F,T,F}, N(0,2) logits with one exact tie",
+    "decode": "decode: B=256 next-token rows, V=128256, levels=3, no echo, N(0,3) logits + one +12 spike per row",
+    "prefill": "prefill echo: B=8, lengths U[64,2048], V=32000, levels=3, all echo, N(0,2.5) logits",
+    "mixed": "mixed ragged: B=64, lengths U[1,512], V=152064, levels=3, echo Bernoulli(0.5), Student-t(3)x2, "
+             "1% -inf, 0.1% rows with a duplicated max",
+    "wide": "wide top-k: B=32, lengths U[128,1024], V=256000, levels=6, all echo, N(0,1) quantised to 1/16",
+}
+
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the row kernel,
+# keyed by workload, valid only while the kernel sources hash to the recorded value.
+# Filled from the captures summarised under profiles/.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "ragged_log_probs_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def algorithmic_bytes(R: int, V: int, W: int, B: int) -> int:
+    """Each scored logits row read once, outputs written once, offsets/tokens read."""
+    return R * V * 4 + R * W * 8 + (B + 1) * 8 + R * 4
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background; rows carry timestamps."""
+    FIELDS = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 11:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[3]), float(parts[4]), parts[7:11]))
+            except Exception:
+                continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        window = "timed region"
+        if not inside and rows:
+            inside = sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:2]
+            window = "nearest samples (timed region shorter than the 100 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------------ oracle leg
+def _oracle_row(args):
+    import oracle
+    row, t, levels = args
+    return oracle.score_row(row, t, levels)[0][0]
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(batch, n_rows: int, seed: int = 0):
+    """Copy n scored rows device->host with their targets (work items for the oracle)."""
+    import numpy as np
+    import oracle
+    off, tokens, sampled, echo = batch.host()
+    mapping = oracle.output_rows(off, echo, tokens, sampled)
+    rng = np.random.default_rng(seed)
+    picks = rng.choice(len(mapping), size=min(n_rows, len(mapping)), replace=False)
+    return [(batch.logits[mapping[o][1]].cpu().numpy(), mapping[o][2], batch.levels) for o in picks]
+
+
+def time_oracle(batch, target_cpu_s: float, pool, cores: int, items=None):
+    """Time the oracle, as it stands, over a bounded row sample on the host cores."""
+    probe = oracle_sample(batch, 1, seed=99)
+    t = time.perf_counter()
+    _oracle_row(probe[0])
+    t_row = max(time.perf_counter() - t, 1e-4)
+    n = int(max(cores, min(4000, target_cpu_s / t_row)))
+    items = oracle_sample(batch, n, seed=1) if items is None else items
+    pool.map(_oracle_row, items[:cores])  # workers import numpy/oracle before timing
+    t0 = time.perf_counter()
+    pool.map(_oracle_row, items, chunksize=1)
+    dt = time.perf_counter() - t0
+    return len(items), dt
+
+
+# -------------------------------------------------------------------------- our arm
+def run_ours(args, rank: int, world: int, dist):
+    import numpy as np
+    import torch
+
+    import ragged_log_probs_gb300 as lp
+    import workloads
+    from ragged_log_probs_gb300 import _build
+
+    _build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    batch = workloads.make_batch(args.config, dev)
+    B, T, V, levels = batch.B, batch.T, batch.V, batch.levels
+    W = lp.out_per_token(levels)
+    ws = lp.new_workspace(B, T, V, levels, dev)
+    host = torch.zeros(2, dtype=torch.int32).pin_memory()
+    out_off = lp.plan(batch.logit_row_offsets, batch.echo, T, ws, host_out=host)
+    torch.cuda.synchronize()
+    R = int(host[0])
+    if int(host[1]) != 0:
+        raise RuntimeError(f"plan status {int(host[1])}")
+    out_lp = torch.empty((R, W), dtype=torch.float32, device=dev)
+    out_tok = torch.empty((R, W), dtype=torch.int32, device=dev)
+
+    # Rotate over enough logits copies that each step reads HBM, not L2.
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or (128 << 20))
+    lbytes = batch.logits.numel() * 4
+    n_copies = max(1, math.ceil(3 * l2 / lbytes))
+    copies = [batch.logits] + [batch.logits.clone() for _ in range(n_copies - 1)]
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        lp.plan(batch.logit_row_offsets, batch.echo, T, ws, output_row_offsets=out_off, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        lp.compute(copies[i % n_copies], batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, out_off,
+                   batch.echo, levels, out_lp, out_tok, ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if lp.read_status(ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # Sanity gate (parity itself is the tests' job): ids in range, logprobs <= 0.
+    tok_np = out_tok.cpu().numpy().view(np.uint32)
+    lp_np = out_lp.cpu().numpy()
+    K = W - 1
+    if np.any(tok_np[:, :K] >= V) or np.any(lp_np[~np.isnan(lp_np)] > 1e-4):
+        raise RuntimeError("output sanity check failed")
+
+    uuid = None
+    try:
+        u = str(props.uuid)
+        uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    # untimed settle so the clock samples see the GPU under load
+    t_settle = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_settle < args.settle_s:
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(k, events[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    sampler.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_step = ms_total / args.steps
+    compute_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
+    if dist is not None:
+        t = torch.tensor([ms_step, compute_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, compute_ms = float(t[0]), float(t[1])
+    clocks = sampler.summary(w0, w1)
+    status = lp.read_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # End to end through the public API: pinned host inputs -> device, plan+compute, results -> host.
+    e2e = None
+    if not args.no_e2e:
+        h_logits = batch.logits.cpu().pin_memory()
+        h_ints = [t.cpu().pin_memory() for t in (batch.logit_row_offsets, batch.tokens, batch.sampled_tokens,
+                                                  batch.echo)]
+        d_logits = torch.empty_like(batch.logits)
+        d_ints = [torch.empty_like(t) for t in (batch.logit_row_offsets, batch.tokens, batch.sampled_tokens,
+                                                batch.echo)]
+        h_lp = torch.empty((R, W), dtype=torch.float32).pin_memory()
+        h_tok = torch.empty((R, W), dtype=torch.int32).pin_memory()
+        h2d = h_logits.numel() * 4 + sum(t.numel() * t.element_size() for t in h_ints)
+        d2h = h_lp.numel() * 4 + h_tok.numel() * 4
+        k_e2e = int(max(3, min(args.steps, 40e9 // max(h2d, 1))))
+
+        def e2e_step():
+            d_logits.copy_(h_logits, non_blocking=True)
+            for d, h in zip(d_ints, h_ints):
+                d.copy_(h, non_blocking=True)
+            lp.plan(d_ints[0], d_ints[3], T, ws, output_row_offsets=out_off, stream=stream)
+            lp.compute(d_logits, d_ints[0], d_ints[1], d_ints[2], out_off, d_ints[3], levels, out_lp, out_tok, ws,
+                       stream=stream)
+            h_lp.copy_(out_lp, non_blocking=True)
+            h_tok.copy_(out_tok, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        ea.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = ea.elapsed_time(eb) / k_e2e
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        e2e = {"value": R * world / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": k_e2e}
+
+    alg = algorithmic_bytes(R, V, W, B)
+    achieved = alg / (compute_ms / 1e3) / 1e9
+    peak, peak_src = measured_peak_hbm()
+    traffic = None
+    rec = NCU_TRAFFIC.get(args.config)
+    if rec and rec.get("source_hash") == kernel_source_hash():
+        traffic = rec["bytes_per_launch"]
+    roofline = {"bound": "hbm", "kernel": "k_rows (lp_ragged_compute)", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
+                "compute_ms_per_launch": round(compute_ms, 5)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import multiprocessing as mp
+        cores = cpu_cores()
+        with mp.get_context("spawn").Pool(cores) as pool:
+            n, dt = time_oracle(batch, args.cpu_seconds, pool, cores)
+        cpu = {"value": n / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} random scored rows of this workload (numpy fp64 oracle, full sort per row), "
+                         f"{dt:.1f} s wall over a spawn pool of {cores} processes"}
+
+    line = {
+        "metric": METRIC, "value": R * world / (ms_step / 1e3), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "B": B, "T": T, "V": V,
+                   "levels": levels, "rows_per_gpu": R, "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": f"inputs larger than L2: {n_copies} rotating logits copies of {lbytes / 1e6:.0f} MB "
+                         f"(L2 {l2 / 1e6:.0f} MB)"},
+        "hbm_gbs_step": round(alg * world / (ms_step / 1e3) / 1e9, 1),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 2 * args.steps, "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- reference arm
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    import multiprocessing as mp
+
+    import torch
+    import workloads
+
+    cores = cpu_cores()
+    with mp.get_context("spawn").Pool(cores) as pool:
+        dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+        batch = workloads.make_batch(args.config, dev)
+        probe = oracle_sample(batch, 1, seed=99)
+        t = time.perf_counter()
+        _oracle_row(probe[0])
+        t_row = max(time.perf_counter() - t, 1e-4)
+        budget_s = 150.0
+        steps_total = args.steps + args.warmup
+        per_step = int(max(1, min(cores * 4, budget_s * cores / (t_row * steps_total))))
+        items = oracle_sample(batch, per_step * 4, seed=1)
+        pool.map(_oracle_row, items[:cores])
+        times = []
+        for k in range(steps_total):
+            work = [items[(k * per_step + j) % len(items)] for j in range(per_step)]
+            t0 = time.perf_counter()
+            pool.map(_oracle_row, work, chunksize=1)
+            if k >= args.warmup:
+                times.append(time.perf_counter() - t0)
+    ms_step = 1e3 * sum(times) / len(times)
+    value = per_step / (ms_step / 1e3)
+    sample = (f"{per_step} random scored rows of the workload per step (numpy fp64 oracle, full sort per row) "
+              f"over a spawn pool of {cores} processes")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "B": batch.B, "T": batch.T,
+                   "V": batch.V, "levels": batch.levels},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="decode", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--settle-s", type=float, default=1.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

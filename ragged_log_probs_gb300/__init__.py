@@ -1,0 +1,219 @@
+"""Ragged batched log-probabilities on GB300: thin Python binding of the C ABI.
+
+Argument marshalling only. Every step of the path (output offsets, the streaming
+max / sum-exp / top-k reduction, the split-row merge, the target gather) runs in
+the CUDA kernels of ``liblp_ragged.so``; there is no CPU or library fallback, and
+importing this package fails loudly when the library has not been built.
+
+Integer tensors may be ``torch.int32`` or ``torch.uint32`` (same bits); echo flags
+``torch.uint8`` or ``torch.bool``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "LpError", "lib_path", "load", "workspace_size", "new_workspace", "plan", "compute",
+    "read_status", "ragged_log_probs", "out_per_token", "STATUS_NAMES",
+]
+
+LP_MAX_LEVELS = 6
+PAD_TOKEN = 0xFFFFFFFF
+STATUS_NAMES = {
+    0: "LP_OK", 1: "LP_ERR_NULL", 2: "LP_ERR_LEVELS", 3: "LP_ERR_SHAPE", 4: "LP_ERR_OFFSETS",
+    5: "LP_ERR_TOKEN_RANGE", 6: "LP_ERR_WORKSPACE", 7: "LP_ERR_CUDA",
+}
+EXPORTS = ("lp_ragged_workspace_size", "lp_ragged_plan", "lp_ragged_compute",
+           "lp_ragged_read_status", "lp_ragged_strerror")
+
+
+class LpError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)} ({_strerror(code)})")
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def lib_path() -> str:
+    return _build.lib_path()
+
+
+def load() -> ctypes.CDLL:
+    """Load ``liblp_ragged.so`` (built by ``__graft_entry__.build()``); raise if absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: run __graft_entry__.build() (nvcc, sm_103a) first")
+    lib = ctypes.CDLL(path)
+    u32, vp, sz = ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t
+    lib.lp_ragged_workspace_size.argtypes = [u32, u32, u32, u32]
+    lib.lp_ragged_workspace_size.restype = sz
+    lib.lp_ragged_plan.argtypes = [vp, vp, u32, u32, vp, vp, vp, sz, vp]
+    lib.lp_ragged_plan.restype = ctypes.c_int
+    lib.lp_ragged_compute.argtypes = [vp, u32, u32, vp, u32, vp, vp, vp, vp, u32, vp, vp, vp, sz, vp]
+    lib.lp_ragged_compute.restype = ctypes.c_int
+    lib.lp_ragged_read_status.argtypes = [vp, vp, vp]
+    lib.lp_ragged_read_status.restype = ctypes.c_int
+    lib.lp_ragged_strerror.argtypes = [ctypes.c_int]
+    lib.lp_ragged_strerror.restype = ctypes.c_char_p
+    _LIB = lib
+    return lib
+
+
+def _strerror(code: int) -> str:
+    try:
+        return load().lp_ragged_strerror(code).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def out_per_token(levels: int) -> int:
+    return 2 ** levels if levels > 0 else 1
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dev_u32(t: torch.Tensor, name: str, n: Optional[int] = None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in (torch.int32, torch.uint32):
+        raise TypeError(f"{name} must be int32/uint32, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if n is not None and t.numel() < n:
+        raise ValueError(f"{name} needs {n} elements, has {t.numel()}")
+    return t.data_ptr()
+
+
+def _dev_u8(t: torch.Tensor, name: str, n: int) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in (torch.uint8, torch.bool, torch.int8):
+        raise TypeError(f"{name} must be uint8/bool, got {t.dtype}")
+    if not t.is_contiguous() or t.numel() < n:
+        raise ValueError(f"{name} must be contiguous with {n} elements")
+    return t.data_ptr()
+
+
+def workspace_size(B: int, T: int, V: int, levels: int) -> int:
+    """Bytes of scratch for one call on the current device."""
+    return int(load().lp_ragged_workspace_size(B, T, V, levels))
+
+
+def new_workspace(B: int, T: int, V: int, levels: int, device=None) -> torch.Tensor:
+    """Allocate a workspace tensor (uint8) on ``device`` (torch allocates; the library never does)."""
+    device = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        n = workspace_size(B, T, V, levels)
+        if n == 0:
+            raise LpError(2 if levels > LP_MAX_LEVELS else 7, "lp_ragged_workspace_size")
+        return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def plan(logit_row_offsets: torch.Tensor, echo: torch.Tensor, T: int, workspace: torch.Tensor,
+         output_row_offsets: Optional[torch.Tensor] = None, host_out: Optional[torch.Tensor] = None,
+         stream=None) -> torch.Tensor:
+    """Enqueue ``lp_ragged_plan``; returns ``output_row_offsets`` (device, B+1).
+
+    ``host_out`` (optional, 2 x int32 on the host, pinned for an async copy) receives
+    ``{R, status bits}`` once the stream has reached this point."""
+    lib = load()
+    B = logit_row_offsets.numel() - 1
+    if output_row_offsets is None:
+        output_row_offsets = torch.empty(B + 1, dtype=logit_row_offsets.dtype, device=logit_row_offsets.device)
+    hp = None
+    if host_out is not None:
+        if host_out.is_cuda or host_out.numel() < 2 or host_out.element_size() != 4 or not host_out.is_contiguous():
+            raise ValueError("host_out must be a contiguous 2-word host tensor")
+        hp = host_out.data_ptr()
+    rc = lib.lp_ragged_plan(_dev_u32(logit_row_offsets, "logit_row_offsets", B + 1), _dev_u8(echo, "echo", B),
+                            B, T, _dev_u32(output_row_offsets, "output_row_offsets", B + 1), hp,
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _stream_handle(stream))
+    if rc:
+        raise LpError(rc, "lp_ragged_plan")
+    return output_row_offsets
+
+
+def compute(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: torch.Tensor,
+            sampled_tokens: torch.Tensor, output_row_offsets: torch.Tensor, echo: torch.Tensor, levels: int,
+            out_logprobs: torch.Tensor, out_tokens: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Enqueue ``lp_ragged_compute`` (outputs must hold R x W entries, R = output_row_offsets[B])."""
+    lib = load()
+    if logits.dim() != 2 or logits.dtype != torch.float32 or not logits.is_cuda:
+        raise TypeError("logits must be a 2-D float32 CUDA tensor")
+    if logits.stride(1) != 1 or logits.stride(0) != logits.shape[1]:
+        raise ValueError("logits must be row-major contiguous")
+    T, V = logits.shape
+    B = logit_row_offsets.numel() - 1
+    if out_logprobs.dtype != torch.float32 or not out_logprobs.is_cuda or not out_logprobs.is_contiguous():
+        raise TypeError("out_logprobs must be a contiguous float32 CUDA tensor")
+    rc = lib.lp_ragged_compute(
+        logits.data_ptr(), T, V, _dev_u32(logit_row_offsets, "logit_row_offsets", B + 1), B,
+        _dev_u32(tokens, "tokens", T), _dev_u32(sampled_tokens, "sampled_tokens", B),
+        _dev_u32(output_row_offsets, "output_row_offsets", B + 1), _dev_u8(echo, "echo", B), levels,
+        out_logprobs.data_ptr(), _dev_u32(out_tokens, "out_tokens"),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc:
+        raise LpError(rc, "lp_ragged_compute")
+
+
+def read_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronously read the device status bits (bit c set <=> error code c seen)."""
+    lib = load()
+    host = torch.zeros(1, dtype=torch.int32).pin_memory()
+    rc = lib.lp_ragged_read_status(workspace.data_ptr(), host.data_ptr(), _stream_handle(stream))
+    if rc:
+        raise LpError(rc, "lp_ragged_read_status")
+    (torch.cuda.current_stream() if stream is None else stream).synchronize()
+    return int(host.item()) & 0xFFFFFFFF
+
+
+def ragged_log_probs(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: torch.Tensor,
+                     sampled_tokens: torch.Tensor, echo: torch.Tensor, levels: int,
+                     workspace: Optional[torch.Tensor] = None, stream=None, check: bool = True):
+    """plan -> size outputs (one host sync for R) -> compute.
+
+    Returns ``(output_row_offsets [B+1], logprobs f32 [R, W], token_ids int32-storage-of-uint32 [R, W])``."""
+    T, V = logits.shape
+    B = logit_row_offsets.numel() - 1
+    if workspace is None:
+        workspace = new_workspace(B, T, V, levels, logits.device)
+    host = torch.zeros(2, dtype=torch.int32).pin_memory()
+    out_off = plan(logit_row_offsets, echo, T, workspace, host_out=host, stream=stream)
+    (torch.cuda.current_stream() if stream is None else stream).synchronize()
+    R, status = int(host[0]), int(host[1]) & 0xFFFFFFFF
+    if status:
+        raise LpError(_first_bit(status), "lp_ragged_plan (device)")
+    W = out_per_token(levels)
+    out_lp = torch.empty((R, W), dtype=torch.float32, device=logits.device)
+    out_tok = torch.empty((R, W), dtype=torch.int32, device=logits.device)
+    compute(logits, logit_row_offsets, tokens, sampled_tokens, out_off, echo, levels, out_lp, out_tok,
+            workspace, stream=stream)
+    if check:
+        status = read_status(workspace, stream)
+        if status:
+            raise LpError(_first_bit(status), "lp_ragged_compute (device)")
+    return out_off, out_lp, out_tok
+
+
+def _first_bit(bits: int) -> int:
+    for c in range(1, 32):
+        if bits & (1 << c):
+            return c
+    return 0

@@ -1,0 +1,138 @@
+// Device helpers for the ragged log-probability kernels (sm_103a).
+//
+// Top-k ordering key, used at every merge level: fp32 logit descending, then token
+// id ascending (ties on equal logits go to the lower id).  A warp keeps a sorted
+// list of 32*SLOTS (logit, id) pairs, slot i = reg (i / 32), lane (i % 32).
+#pragma once
+
+#include <cstdint>
+
+namespace lpk {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kPadId = 0xFFFFFFFFu;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// 2^x with the SFU (PTX ex2.approx; -inf -> +0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Streaming 16-byte load: read-only path, no L1 allocation, 256-byte L2 prefetch.
+__device__ __forceinline__ float4 ldg_stream(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ bool better(float xa, uint32_t ia, float xb, uint32_t ib) {
+    return xa > xb || (xa == xb && ia < ib);
+}
+
+// Order-preserving map float -> uint32 (for atomicMax on a shared threshold).
+__device__ __forceinline__ uint32_t f2ord(float f) {
+    uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord2f(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+__device__ __forceinline__ float pick(const float4& v, int k) {
+    return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ uint32_t ge_mask(const float4& v, float thr) {
+    return (uint32_t)(v.x >= thr) | ((uint32_t)(v.y >= thr) << 1) | ((uint32_t)(v.z >= thr) << 2) |
+           ((uint32_t)(v.w >= thr) << 3);
+}
+
+// Descending bitonic merge of a bitonic 32-sequence held one element per lane.
+__device__ __forceinline__ void bitonic_merge32(float& x, uint32_t& id, int lane) {
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        float ox = __shfl_xor_sync(kFull, x, j);
+        uint32_t oid = __shfl_xor_sync(kFull, id, j);
+        bool lower = (lane & j) == 0;
+        bool ob = better(ox, oid, x, id);
+        if (ob == lower) { x = ox; id = oid; }
+    }
+}
+
+// Descending bitonic sort of 32 arbitrary pairs, one per lane.
+__device__ __forceinline__ void bitonic_sort32(float& x, uint32_t& id, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            float ox = __shfl_xor_sync(kFull, x, j);
+            uint32_t oid = __shfl_xor_sync(kFull, id, j);
+            bool lower = (lane & j) == 0;
+            bool desc = (lane & k) == 0;
+            bool ob = better(ox, oid, x, id);
+            bool take = (lower == desc) ? ob : !ob;
+            if (take) { x = ox; id = oid; }
+        }
+    }
+}
+
+// a := best 32*SLOTS of (a U b); both sorted descending in the lane-major layout.
+template <int SLOTS>
+__device__ __forceinline__ void merge_lists(float (&ax)[SLOTS], uint32_t (&ai)[SLOTS],
+                                            const float (&bx)[SLOTS], const uint32_t (&bi)[SLOTS],
+                                            int lane) {
+    static_assert(SLOTS == 1 || SLOTS == 2, "one or two slots per lane");
+    const int src = 31 - lane;
+    if constexpr (SLOTS == 1) {
+        float rx = __shfl_sync(kFull, bx[0], src);
+        uint32_t ri = __shfl_sync(kFull, bi[0], src);
+        if (better(rx, ri, ax[0], ai[0])) { ax[0] = rx; ai[0] = ri; }
+        bitonic_merge32(ax[0], ai[0], lane);
+    } else {
+        // position i of the 64-list pairs with position 63-i of b:
+        // slot lane <-> b slot 32+(31-lane); slot 32+lane <-> b slot (31-lane).
+        float r1x = __shfl_sync(kFull, bx[1], src);
+        uint32_t r1i = __shfl_sync(kFull, bi[1], src);
+        float r0x = __shfl_sync(kFull, bx[0], src);
+        uint32_t r0i = __shfl_sync(kFull, bi[0], src);
+        float c0x = ax[0], c1x = ax[1];
+        uint32_t c0i = ai[0], c1i = ai[1];
+        if (better(r1x, r1i, c0x, c0i)) { c0x = r1x; c0i = r1i; }
+        if (better(r0x, r0i, c1x, c1i)) { c1x = r0x; c1i = r0i; }
+        // half-cleaner at distance 32 (same lane, two registers)
+        if (better(c1x, c1i, c0x, c0i)) {
+            float tx = c0x; c0x = c1x; c1x = tx;
+            uint32_t ti = c0i; c0i = c1i; c1i = ti;
+        }
+        bitonic_merge32(c0x, c0i, lane);
+        bitonic_merge32(c1x, c1i, lane);
+        ax[0] = c0x; ai[0] = c0i;
+        ax[1] = c1x; ai[1] = c1i;
+    }
+}
+
+// Combine two (max, sum of exp(x - max)) pairs.
+__device__ __forceinline__ void lse_combine(float& m, float& s, float om, float os) {
+    float M = fmaxf(m, om);
+    float a = (m == neg_inf()) ? 0.f : s * ex2((m - M) * kLog2e);
+    float b = (om == neg_inf()) ? 0.f : os * ex2((om - M) * kLog2e);
+    m = M;
+    s = a + b;
+}
+
+__device__ __forceinline__ void warp_lse_reduce(float& m, float& s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float om = __shfl_xor_sync(kFull, m, o);
+        float os = __shfl_xor_sync(kFull, s, o);
+        lse_combine(m, s, om, os);
+    }
+}
+
+}  // namespace lpk

@@ -1,0 +1,206 @@
+// C ABI of the ragged log-probability library (declared in include/lp_ragged.h).
+//
+// Host side: argument checks, launch-shape choice (persistent grid = SMs x
+// resident CTAs), and the workspace layout. Every step of the path runs in the
+// kernels of lp_kernels.cuh.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "lp_kernels.cuh"
+#include "lp_ragged.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint32_t kMaxCtasPerSm = 8;
+constexpr uint32_t kMinPieceVec = 2048;         // 32 KB of logits per CTA at least
+constexpr uint32_t kStageOffsetsMax = 2048;     // stage off/out_off in smem when B+1 <= this
+constexpr uint32_t kUnroll = 4;
+constexpr int kVariants = 3;                    // levels 0 | 1..5 | 6
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int occ[kVariants] = {0, 0, 0};
+    size_t occ_smem[kVariants] = {0, 0, 0};
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+const void* variant_fn(int v) {
+    switch (v) {
+        case 0: return reinterpret_cast<const void*>(&lpk::k_rows<1, false, kUnroll>);
+        case 1: return reinterpret_cast<const void*>(&lpk::k_rows<1, true, kUnroll>);
+        default: return reinterpret_cast<const void*>(&lpk::k_rows<2, true, kUnroll>);
+    }
+}
+
+int variant_of(uint32_t levels) { return levels == 0 ? 0 : (levels < 6 ? 1 : 2); }
+
+bool device_info(int* dev_out, DeviceInfo** info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            return false;
+        d.sms = sms;
+        d.ready = true;
+    }
+    *dev_out = dev;
+    *info = &d;
+    return true;
+}
+
+int occupancy(DeviceInfo* d, int v, size_t smem) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (d->occ[v] == 0 || d->occ_smem[v] != smem) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, variant_fn(v), lpk::kThreads, smem) != cudaSuccess)
+            n = 1;
+        if (n < 1) n = 1;
+        if (n > (int)kMaxCtasPerSm) n = kMaxCtasPerSm;
+        d->occ[v] = n;
+        d->occ_smem[v] = smem;
+    }
+    return d->occ[v];
+}
+
+size_t counters_bytes(uint32_t g_max) { return ((size_t)g_max * 4 + 255) & ~(size_t)255; }
+
+size_t workspace_bytes_for(int sms, uint32_t levels) {
+    const uint32_t K = (1u << levels) - 1u;
+    const uint32_t g_max = (uint32_t)sms * kMaxCtasPerSm;
+    return sizeof(lpk::WsHeader) + counters_bytes(g_max) + (size_t)2 * g_max * lpk::partial_stride_bytes(K);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lp_ragged_workspace_size(uint32_t B, uint32_t T, uint32_t V, uint32_t levels) {
+    (void)B; (void)T; (void)V;
+    if (levels > LP_MAX_LEVELS) return 0;
+    int dev;
+    DeviceInfo* d;
+    if (!device_info(&dev, &d)) return 0;
+    return workspace_bytes_for(d->sms, levels);
+}
+
+lp_status lp_ragged_plan(const uint32_t* logit_row_offsets, const uint8_t* echo, uint32_t B, uint32_t T,
+                         uint32_t* output_row_offsets, uint32_t* host_rows_and_status, void* workspace,
+                         size_t workspace_bytes, lp_stream_t stream) {
+    if (!logit_row_offsets || !echo || !output_row_offsets) return LP_ERR_NULL;
+    if (!workspace) return LP_ERR_WORKSPACE;
+    if (B == 0 || T == 0) return LP_ERR_SHAPE;
+    if (((uintptr_t)workspace & 255u) != 0) return LP_ERR_WORKSPACE;
+    int dev;
+    DeviceInfo* d;
+    if (!device_info(&dev, &d)) return LP_ERR_CUDA;
+    const uint32_t g_max = (uint32_t)d->sms * kMaxCtasPerSm;
+    if (workspace_bytes < sizeof(lpk::WsHeader) + counters_bytes(g_max)) return LP_ERR_WORKSPACE;
+    auto* hdr = static_cast<lpk::WsHeader*>(workspace);
+    auto* counters = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) + sizeof(lpk::WsHeader));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    lpk::k_plan<<<1, lpk::kPlanThreads, 0, s>>>(logit_row_offsets, echo, B, T, output_row_offsets, hdr, counters,
+                                               g_max);
+    if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
+    if (host_rows_and_status) {
+        // header words {status, rows} -> host {rows, status}
+        if (cudaMemcpyAsync(host_rows_and_status, &hdr->rows, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaMemcpyAsync(host_rows_and_status + 1, &hdr->status, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return LP_ERR_CUDA;
+    }
+    return LP_OK;
+}
+
+lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const uint32_t* logit_row_offsets,
+                            uint32_t B, const uint32_t* tokens, const uint32_t* sampled_tokens,
+                            const uint32_t* output_row_offsets, const uint8_t* echo, uint32_t levels,
+                            float* out_logprobs, uint32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                            lp_stream_t stream) {
+    if (!logits || !logit_row_offsets || !tokens || !sampled_tokens || !output_row_offsets || !echo ||
+        !out_logprobs || !out_tokens)
+        return LP_ERR_NULL;
+    if (!workspace) return LP_ERR_WORKSPACE;
+    if (levels > LP_MAX_LEVELS) return LP_ERR_LEVELS;
+    if (B == 0 || T == 0 || V == 0 || V >= 0x7FFFFFFFu) return LP_ERR_SHAPE;
+    if (((uintptr_t)logits & 3u) != 0) return LP_ERR_SHAPE;
+    if (((uintptr_t)workspace & 255u) != 0) return LP_ERR_WORKSPACE;
+    int dev;
+    DeviceInfo* d;
+    if (!device_info(&dev, &d)) return LP_ERR_CUDA;
+    if (workspace_bytes < workspace_bytes_for(d->sms, levels)) return LP_ERR_WORKSPACE;
+
+    const uint32_t K = (1u << levels) - 1u;
+    const uint32_t W = levels ? (1u << levels) : 1u;
+    const uint32_t g_max = (uint32_t)d->sms * kMaxCtasPerSm;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+
+    lpk::RowsParams p;
+    p.logits = logits;
+    p.off = logit_row_offsets;
+    p.tokens = tokens;
+    p.sampled = sampled_tokens;
+    p.out_off = output_row_offsets;
+    p.echo = echo;
+    p.out_lp = out_logprobs;
+    p.out_tok = out_tokens;
+    p.status = &reinterpret_cast<lpk::WsHeader*>(ws)->status;
+    p.counters = reinterpret_cast<uint32_t*>(ws + sizeof(lpk::WsHeader));
+    p.partials = ws + sizeof(lpk::WsHeader) + counters_bytes(g_max);
+    p.T = T;
+    p.V = V;
+    p.B = B;
+    p.K = K;
+    p.W = W;
+    const bool aligned = (((uintptr_t)logits & 15u) == 0) && (V % 4u == 0);
+    p.nq = aligned ? V / 4u : (V + 6u) / 4u;
+    p.stride = lpk::partial_stride_bytes(K);
+    p.min_piece = kMinPieceVec;
+    p.stage_offsets = (B + 1u <= kStageOffsetsMax) ? 1u : 0u;
+    const size_t smem = p.stage_offsets ? (size_t)2 * (B + 1u) * sizeof(uint32_t) : 0;
+
+    const int v = variant_of(levels);
+    const int occ = occupancy(d, v, smem);
+    uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;
+    if (grid > g_max) grid = g_max;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (v) {
+        case 0: lpk::k_rows<1, false, kUnroll><<<grid, lpk::kThreads, smem, s>>>(p); break;
+        case 1: lpk::k_rows<1, true, kUnroll><<<grid, lpk::kThreads, smem, s>>>(p); break;
+        default: lpk::k_rows<2, true, kUnroll><<<grid, lpk::kThreads, smem, s>>>(p); break;
+    }
+    if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
+    return LP_OK;
+}
+
+lp_status lp_ragged_read_status(const void* workspace, uint32_t* host_status, lp_stream_t stream) {
+    if (!workspace || !host_status) return LP_ERR_NULL;
+    const auto* hdr = static_cast<const lpk::WsHeader*>(workspace);
+    if (cudaMemcpyAsync(host_status, &hdr->status, 4, cudaMemcpyDeviceToHost,
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LP_ERR_CUDA;
+    return LP_OK;
+}
+
+const char* lp_ragged_strerror(lp_status status) {
+    switch (status) {
+        case LP_OK: return "ok";
+        case LP_ERR_NULL: return "a required pointer is NULL";
+        case LP_ERR_LEVELS: return "levels exceeds 6 (top-k capacity 63)";
+        case LP_ERR_SHAPE: return "B, T or V is zero or too large, or logits are not 4-byte aligned";
+        case LP_ERR_OFFSETS: return "row offsets invalid: empty/decreasing batch, range past T, or echo mismatch";
+        case LP_ERR_TOKEN_RANGE: return "an actual or sampled token id is >= V";
+        case LP_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case LP_ERR_CUDA: return "CUDA launch or copy failed";
+        default: return "unknown lp_status";
+    }
+}
+
+}  // extern "C"

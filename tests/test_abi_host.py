@@ -1,0 +1,92 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every symbol
+the header declares, and rejects bad arguments on the host (no kernel runs)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lp_ragged.h")
+
+LP_OK, LP_ERR_NULL, LP_ERR_LEVELS, LP_ERR_SHAPE = 0, 1, 2, 3
+LP_ERR_OFFSETS, LP_ERR_TOKEN_RANGE, LP_ERR_WORKSPACE, LP_ERR_CUDA = 4, 5, 6, 7
+FAKE = 0x10000          # non-NULL, 256-byte aligned, never dereferenced: each call returns first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ragged_log_probs_gb300 import _build
+    _build.build()
+    import ragged_log_probs_gb300 as lp
+    return lp.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(lp_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    assert set(declared_functions()) >= {"lp_ragged_workspace_size", "lp_ragged_plan", "lp_ragged_compute",
+                                         "lp_ragged_read_status", "lp_ragged_strerror"}
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_strerror_covers_codes(lib):
+    seen = set()
+    for code in range(8):
+        s = lib.lp_ragged_strerror(code).decode()
+        assert s and s != "unknown lp_status"
+        seen.add(s)
+    assert len(seen) == 8
+    assert lib.lp_ragged_strerror(99).decode() == "unknown lp_status"
+
+
+def _compute(lib, logits=FAKE, T=4, V=100, off=FAKE, B=2, tokens=FAKE, sampled=FAKE, out_off=FAKE, echo=FAKE,
+             levels=3, out_lp=FAKE, out_tok=FAKE, ws=FAKE, ws_bytes=1 << 20):
+    return lib.lp_ragged_compute(logits, T, V, off, B, tokens, sampled, out_off, echo, levels, out_lp, out_tok,
+                                 ws, ws_bytes, None)
+
+
+def test_compute_host_checks(lib):
+    assert _compute(lib, logits=None) == LP_ERR_NULL
+    assert _compute(lib, tokens=None) == LP_ERR_NULL
+    assert _compute(lib, out_tok=None) == LP_ERR_NULL
+    assert _compute(lib, ws=None) == LP_ERR_WORKSPACE
+    assert _compute(lib, levels=7) == LP_ERR_LEVELS
+    assert _compute(lib, V=0) == LP_ERR_SHAPE
+    assert _compute(lib, B=0) == LP_ERR_SHAPE
+    assert _compute(lib, T=0) == LP_ERR_SHAPE
+    assert _compute(lib, V=0x7FFFFFFF) == LP_ERR_SHAPE
+    assert _compute(lib, logits=FAKE + 2) == LP_ERR_SHAPE
+    assert _compute(lib, ws=FAKE + 16) == LP_ERR_WORKSPACE
+
+
+def test_plan_host_checks(lib):
+    plan = lib.lp_ragged_plan
+    assert plan(None, FAKE, 2, 4, FAKE, None, FAKE, 1 << 20, None) == LP_ERR_NULL
+    assert plan(FAKE, None, 2, 4, FAKE, None, FAKE, 1 << 20, None) == LP_ERR_NULL
+    assert plan(FAKE, FAKE, 2, 4, None, None, FAKE, 1 << 20, None) == LP_ERR_NULL
+    assert plan(FAKE, FAKE, 2, 4, FAKE, None, None, 1 << 20, None) == LP_ERR_WORKSPACE
+    assert plan(FAKE, FAKE, 0, 4, FAKE, None, FAKE, 1 << 20, None) == LP_ERR_SHAPE
+    assert plan(FAKE, FAKE, 2, 0, FAKE, None, FAKE, 1 << 20, None) == LP_ERR_SHAPE
+
+
+def test_read_status_and_workspace_size_host_checks(lib):
+    assert lib.lp_ragged_read_status(None, FAKE, None) == LP_ERR_NULL
+    assert lib.lp_ragged_read_status(FAKE, None, None) == LP_ERR_NULL
+    assert lib.lp_ragged_workspace_size(2, 4, 100, 7) == 0
+
+
+def test_package_fails_loudly_without_library(monkeypatch, tmp_path):
+    import ragged_log_probs_gb300 as lp
+    monkeypatch.setattr(lp, "_LIB", None)
+    monkeypatch.setattr(lp._build, "lib_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        lp.load()

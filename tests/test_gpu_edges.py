@@ -1,0 +1,155 @@
+"""Edge cases of the CUDA path against the oracle: padding (V < K), ties, -inf,
+misaligned rows and base pointers, rows split over many CTAs, device-side errors."""
+
+import numpy as np
+import pytest
+import torch
+
+import ragged_log_probs_gb300 as lp
+import workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    parity.ensure_built()
+
+
+def _custom(logits, lengths, echo, levels, seed=0, **kw):
+    return workloads.make_custom_batch(logits.cuda().contiguous(), lengths, echo, levels, seed=seed, **kw)
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 5, 7, 9])
+@pytest.mark.parametrize("levels", [3, 6])
+def test_vocab_smaller_than_k_pads(V, levels):
+    g = torch.Generator().manual_seed(V)
+    x = torch.randn(6, V, generator=g) * 2
+    b = _custom(x, [2, 3, 1], [1, 0, 1], levels, seed=V)
+    parity.check_batch(b)
+    _, _, tok = parity.run_gpu(b)
+    K = 2 ** levels - 1
+    if V < K:
+        assert np.all(tok[:, V:K] == 0xFFFFFFFF)
+
+
+def test_all_equal_rows():
+    x = torch.full((5, 3001), 0.75)
+    b = _custom(x, [5], [1], 6)
+    parity.check_batch(b)
+    _, out_lp, tok = parity.run_gpu(b)
+    assert tok[:, :63].tolist() == [list(range(63))] * 5
+    np.testing.assert_allclose(out_lp, -np.log(3001), atol=1e-5)
+
+
+def test_quantised_ties_everywhere():
+    g = torch.Generator().manual_seed(3)
+    x = torch.round(torch.randn(40, 20000, generator=g) * 4) / 4
+    b = _custom(x, [10, 30], [1, 1], 6)
+    parity.check_batch(b)
+
+
+def test_neg_inf_rows():
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn(6, 1000, generator=g)
+    x[0, :] = float("-inf")                      # all -inf: NaN logprobs, ids by order rule
+    x[1, 3:] = float("-inf")                      # fewer finite entries than K
+    x[2, ::2] = float("-inf")
+    x[3, 500] = 40.0                              # one dominant entry
+    b = _custom(x, [6], [1], 3)
+    parity.check_batch(b)
+
+
+@pytest.mark.parametrize("V", [4093, 4094, 4095, 4097, 32001])
+def test_odd_vocab_misaligned_rows(V):
+    g = torch.Generator().manual_seed(V)
+    x = torch.randn(9, V, generator=g) * 2
+    b = _custom(x, [4, 1, 4], [1, 0, 1], 3)
+    parity.check_batch(b)
+
+
+@pytest.mark.parametrize("shift", [1, 2, 3])
+def test_misaligned_base_pointer(shift):
+    T, V = 7, 8000
+    g = torch.Generator().manual_seed(shift)
+    flat = torch.empty(T * V + 4, device="cuda")
+    x = flat[shift:shift + T * V].view(T, V)
+    x.copy_((torch.randn(T, V, generator=g) * 2).cuda())
+    assert x.data_ptr() % 16 != 0
+    b = workloads.make_custom_batch(x, [3, 4], [1, 1], 3, seed=shift)
+    parity.check_batch(b)
+
+
+@pytest.mark.parametrize("B,V,levels", [(1, 256000, 6), (1, 128256, 3), (3, 152064, 3), (2, 1000003, 3),
+                                        (1, 5000, 0), (5, 777777, 6)])
+def test_rows_split_over_many_ctas(B, V, levels):
+    b = workloads.make_next_token_batch(B, V, levels=levels, dist="normal", scale=3.0, device="cuda", seed=V)
+    parity.check_batch(b)
+
+
+def test_split_path_repeatable_counters_reset():
+    b = workloads.make_next_token_batch(3, 200000, levels=3, device="cuda", seed=9)
+    ws = lp.new_workspace(b.B, b.T, b.V, b.levels)
+    first = parity.run_gpu(b, workspace=ws)
+    for _ in range(3):
+        again = parity.run_gpu(b, workspace=ws)
+        for x, y in zip(first, again):
+            assert np.array_equal(x, y, equal_nan=True) if x.dtype.kind == "f" else np.array_equal(x, y)
+
+
+def test_single_token_sequences_and_b1():
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(1, 777, generator=g)
+    parity.check_batch(_custom(x, [1], [1], 3))
+    parity.check_batch(_custom(x, [1], [0], 3))
+    x = torch.randn(4, 777, generator=g)
+    parity.check_batch(_custom(x, [1, 1, 1, 1], [1, 0, 1, 0], 2))
+
+
+def test_many_batches_global_offsets_path():
+    # B+1 above the shared-memory staging limit: offsets are read from global memory.
+    B = 3000
+    g = torch.Generator().manual_seed(6)
+    x = torch.randn(B + 100, 64, generator=g)
+    lengths = [1] * (B - 1) + [101]
+    echo = [i % 3 == 0 for i in range(B)]
+    parity.check_batch(_custom(x, lengths, echo, 3))
+
+
+def test_token_out_of_range_sets_status_and_nan():
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(4, 300, generator=g)
+    b = _custom(x, [4], [1], 3, tokens=[1, 2, 300, 3], sampled=[5])
+    ws = lp.new_workspace(b.B, b.T, b.V, b.levels)
+    out_off = lp.plan(b.logit_row_offsets, b.echo, b.T, ws)
+    out_lp = torch.empty((4, 8), device="cuda")
+    out_tok = torch.empty((4, 8), dtype=torch.int32, device="cuda")
+    lp.compute(b.logits, b.logit_row_offsets, b.tokens, b.sampled_tokens, out_off, b.echo, 3, out_lp, out_tok, ws)
+    status = lp.read_status(ws)
+    assert status == (1 << 5)
+    olp = out_lp.cpu().numpy()
+    otok = out_tok.cpu().numpy().view(np.uint32)
+    assert np.isnan(olp[1, 7]) and otok[1, 7] == 300          # row 1 scores token index 2 (= 300)
+    assert not np.isnan(olp[0, 7]) and not np.isnan(olp[2, 7])
+    ref = parity.oracle_for(b)
+    assert not ref[3]
+    parity.compare(olp, otok.astype(np.uint64), ref[1], ref[2], "token range")
+
+
+def test_bad_offsets_detected_on_device():
+    x = torch.randn(6, 100).cuda()
+    off = torch.tensor([0, 3, 3, 6], dtype=torch.int32, device="cuda")   # empty batch 1
+    echo = torch.ones(3, dtype=torch.uint8, device="cuda")
+    ws = lp.new_workspace(3, 6, 100, 3)
+    host = torch.zeros(2, dtype=torch.int32).pin_memory()
+    lp.plan(off, echo, 6, ws, host_out=host)
+    torch.cuda.synchronize()
+    assert int(host[1]) == (1 << 4)
+    off2 = torch.tensor([0, 3, 7], dtype=torch.int32, device="cuda")      # past T
+    lp.plan(off2, echo[:2], 6, ws, host_out=host)
+    torch.cuda.synchronize()
+    assert int(host[1]) == (1 << 4)
+    with pytest.raises(lp.LpError):
+        lp.ragged_log_probs(x, off, torch.zeros(6, dtype=torch.int32, device="cuda"),
+                            torch.zeros(3, dtype=torch.int32, device="cuda"), echo, 3)
