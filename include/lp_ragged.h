@@ -116,6 +116,33 @@ lp_status lp_ragged_compute(const float *logits, uint32_t T, uint32_t V,
                             float *out_logprobs, uint32_t *out_tokens,
                             void *workspace, size_t workspace_bytes, lp_stream_t stream);
 
+/*
+ * Allocation-free form of lp_ragged_compute (no counterpart on the pages; it exists
+ * for callers that cannot allocate device memory: a serving engine whose HBM is
+ * reserved up front by its own pool and that forbids cudaMalloc on the request
+ * path, where cudaMalloc may synchronise the device; or a binding with no device
+ * allocator of its own).
+ *   Same arguments and checks as lp_ragged_compute, minus the workspace. The
+ *   scratch is a static device array of LP_NOALLOC_SCRATCH_BYTES inside this
+ *   library, held by every GPU that loads it until the process exits.
+ *   host_status  optional host word (pinned for an async copy): the status bits of
+ *                this call, valid once the stream reaches this point; NULL skips.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture. Each call zeroes the status word and arrival counters first, and no
+ *   allocating routine (cudaMalloc, cudaFree, a library allocator) is called.
+ *   Returns LP_ERR_WORKSPACE when this GPU needs more scratch than the array holds
+ *   (more than ~300 SMs at levels 6). All calls share the array: calls that overlap
+ *   on the GPU (other streams, other host threads) race; serialise them.
+ */
+#define LP_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
+lp_status lp_ragged_compute_noalloc(const float *logits, uint32_t T, uint32_t V,
+                                    const uint32_t *logit_row_offsets, uint32_t B,
+                                    const uint32_t *tokens, const uint32_t *sampled_tokens,
+                                    const uint32_t *output_row_offsets, const uint8_t *echo, uint32_t levels,
+                                    float *out_logprobs, uint32_t *out_tokens, uint32_t *host_status,
+                                    lp_stream_t stream);
+
 /* Enqueue a copy of the workspace status word (bit c <=> lp_status c) to host. */
 lp_status lp_ragged_read_status(const void *workspace, uint32_t *host_status, lp_stream_t stream);
 

@@ -204,3 +204,74 @@ const char* lp_ragged_strerror(lp_status status) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------
+// Allocation-free variant of lp_ragged_compute.
+//
+// Its scratch (status word, per-CTA arrival counters, split-row partial tuples)
+// lives in one file-scope device array instead of a caller-provided workspace.
+// Every GPU that loads this library holds the array until the process exits; all
+// calls on a device share it, so calls that overlap on the GPU (two streams, two
+// threads) race and corrupt each other's results.
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[LP_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device. Host code cannot use
+// the symbol itself (on the host it names a stand-in object, not device memory).
+// Resolved once per device, on the first call made with that device current.
+bool noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return true;
+}
+
+}  // namespace
+
+extern "C" lp_status lp_ragged_compute_noalloc(const float* logits, uint32_t T, uint32_t V,
+                                               const uint32_t* logit_row_offsets, uint32_t B,
+                                               const uint32_t* tokens, const uint32_t* sampled_tokens,
+                                               const uint32_t* output_row_offsets, const uint8_t* echo,
+                                               uint32_t levels, float* out_logprobs, uint32_t* out_tokens,
+                                               uint32_t* host_status, lp_stream_t stream) {
+    if (!logits || !logit_row_offsets || !tokens || !sampled_tokens || !output_row_offsets || !echo ||
+        !out_logprobs || !out_tokens)
+        return LP_ERR_NULL;
+    if (levels > LP_MAX_LEVELS) return LP_ERR_LEVELS;
+    int dev;
+    DeviceInfo* d;
+    if (!device_info(&dev, &d)) return LP_ERR_CUDA;
+    const size_t need = workspace_bytes_for(d->sms, levels);
+    if (need > (size_t)LP_NOALLOC_SCRATCH_BYTES) return LP_ERR_WORKSPACE;  // GPU has too many SMs for it
+    void* scratch = nullptr;
+    if (!noalloc_scratch(dev, &scratch)) return LP_ERR_CUDA;
+    // The array keeps the previous call's contents: zero the status word and the
+    // arrival counters (the partial tuples are always written before they are read).
+    const uint32_t g_max = (uint32_t)d->sms * kMaxCtasPerSm;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, sizeof(lpk::WsHeader) + counters_bytes(g_max), s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return LP_ERR_CUDA;
+    }
+    const lp_status st = lp_ragged_compute(logits, T, V, logit_row_offsets, B, tokens, sampled_tokens,
+                                           output_row_offsets, echo, levels, out_logprobs, out_tokens, scratch,
+                                           LP_NOALLOC_SCRATCH_BYTES, stream);
+    if (st != LP_OK) return st;
+    if (host_status) {
+        if (cudaMemcpyAsync(host_status, &static_cast<lpk::WsHeader*>(scratch)->status, 4, cudaMemcpyDeviceToHost,
+                            s) != cudaSuccess)
+            return LP_ERR_CUDA;
+    }
+    return LP_OK;
+}
