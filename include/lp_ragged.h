@@ -132,10 +132,10 @@ lp_status lp_ragged_compute(const float *logits, uint32_t T, uint32_t V,
  *   capture. Each call zeroes the status word and arrival counters first, and no
  *   allocating routine (cudaMalloc, cudaFree, a library allocator) is called.
  *   Returns LP_ERR_WORKSPACE when this GPU needs more scratch than the array holds
- *   (more than ~300 SMs at levels 6). All calls share the array: calls that overlap
+ *   (more than ~230 SMs at levels 6). All calls share the array: calls that overlap
  *   on the GPU (other streams, other host threads) race; serialise them.
  */
-#define LP_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
+#define LP_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 lp_status lp_ragged_compute_noalloc(const float *logits, uint32_t T, uint32_t V,
                                     const uint32_t *logit_row_offsets, uint32_t B,
                                     const uint32_t *tokens, const uint32_t *sampled_tokens,

@@ -44,17 +44,20 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile the library if a source changed; return its path."""
-    out = lib_path()
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, out: str | None = None,
+          defines=()) -> str:
+    """Compile the library if a source changed; return its path. ``defines`` (e.g.
+    ``["LP_UNROLL=8"]``) override the kernel's tuning knobs; use with ``out``."""
+    out = out or lib_path()
+    if not force and not defines and out == lib_path() and up_to_date():
         return out
-    os.makedirs(LIB_DIR, exist_ok=True)
+    os.makedirs(os.path.dirname(os.path.abspath(out)), exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
     cmd = [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-O2",
            "-I", INCLUDE, "-I", CSRC, "-o", tmp]
     if ptxas_verbose:
         cmd += ["-Xptxas", "-v"]
+    cmd += [f"-D{d}" for d in defines]
     cmd += [os.path.join(CSRC, f) for f in SOURCES]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)

@@ -117,6 +117,34 @@ __device__ __forceinline__ void merge_lists(float (&ax)[SLOTS], uint32_t (&ai)[S
     }
 }
 
+// max(a, b, c) in one instruction (three-source max, sm_100+).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float max4(const float4& v) { return fmaxf(max3(v.x, v.y, v.z), v.w); }
+
+// Combine two (reference c, sum of 2^(x*log2e - c)) pairs in the log2 domain;
+// c == -inf marks an empty sum.
+__device__ __forceinline__ void lse2_combine(float& c, float& s, float oc, float os) {
+    float C = fmaxf(c, oc);
+    float a = (c == neg_inf()) ? 0.f : s * ex2(c - C);
+    float b = (oc == neg_inf()) ? 0.f : os * ex2(oc - C);
+    c = C;
+    s = a + b;
+}
+
+__device__ __forceinline__ void warp_lse2_reduce(float& c, float& s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float oc = __shfl_xor_sync(kFull, c, o);
+        float os = __shfl_xor_sync(kFull, s, o);
+        lse2_combine(c, s, oc, os);
+    }
+}
+
 // Combine two (max, sum of exp(x - max)) pairs.
 __device__ __forceinline__ void lse_combine(float& m, float& s, float om, float os) {
     float M = fmaxf(m, om);

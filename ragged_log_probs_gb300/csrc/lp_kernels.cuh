@@ -2,12 +2,25 @@
 //
 //  k_plan   one CTA: output_row_offsets = [0, cumsum(echo ? len : 1)], validation,
 //           clears the workspace status word and arrival counters.
-//  k_rows   persistent stream-K reduction over all scored logits rows.
+//  k_rows   persistent, warp-granular stream-K reduction over all scored logits rows.
 //
 // The operation follows "MAX Python SDK 中 log_probabilities 模块解析" (sections
 // "ragged 数据编排：从输入缓冲到 kernel 调用" and "top-k 语义：堆式 kernel 与「采样
 // token 兜底」") and the logprob definition of "logprob、finish reason 与 output
 // processing" (section "logprob 的数值形态").
+//
+// Work split. The scored rows form a vector space of R * nq 16-byte vectors (row o,
+// vector q). Warp g of the grid owns the contiguous range [start(g), start(g+1)) of
+// that space. A row that falls inside one warp's range is finished by that warp
+// alone; a row cut by range boundaries is processed as pieces by consecutive warps,
+// each of which stores a partial tuple (reference, sum, top-k, target logit) and
+// takes a ticket; the warp that takes the last ticket merges the pieces and writes
+// the row. Nothing waits on another warp, so there is no inter-warp spin.
+//
+// Sum-exp in the log2 domain. A lane keeps m (largest logit seen), c = m*log2(e)
+// rounded to fp32, and s = sum 2^(x*log2(e) - c): one FFMA, one EX2 and one FADD per
+// logit. Then lse = c*ln2 + ln(s) (evaluated in fp64); the only approximation beyond
+// rounding is the fp32 value of log2(e), which scales the logits by 1 - 1.3e-8.
 #pragma once
 
 #include <cstdint>
@@ -16,13 +29,23 @@
 
 namespace lpk {
 
+// Tuning knobs (compile-time): 16-byte vectors per lane per block, and the minimum
+// resident CTAs per SM the register budget is cut for.
+#ifndef LP_UNROLL
+#define LP_UNROLL 4
+#endif
+#ifndef LP_MIN_BLOCKS
+#define LP_MIN_BLOCKS 3
+#endif
+
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kPlanThreads = 1024;
 constexpr uint32_t kStatusOffsets = 1u << 4;     // bit of LP_ERR_OFFSETS
 constexpr uint32_t kStatusTokenRange = 1u << 5;  // bit of LP_ERR_TOKEN_RANGE
+constexpr double kLn2 = 0.69314718055994530942;
 
-// Workspace: [header 256 B][counters u32 x g_max, padded to 256 B][partial slots].
+// Workspace: [header 256 B][counters u32 x max warps, padded to 256 B][partial slots].
 struct WsHeader {
     uint32_t status;
     uint32_t rows;
@@ -30,7 +53,7 @@ struct WsHeader {
 };
 
 // Partial tuple of one piece of a split row (u32 words):
-//   [0] max  [1] sum-exp  [2] target logit  [3] 1 if [2] is valid
+//   [0] reference c  [1] sum s  [2] target logit  [3] 1 if [2] is valid
 //   [4, 4+K) top-k logits (sorted)   [4+K, 4+2K) their ids
 __host__ __device__ inline uint32_t partial_stride_bytes(uint32_t K) {
     return ((4u + 2u * K) * 4u + 15u) & ~15u;
@@ -49,10 +72,10 @@ struct RowsParams {
     uint32_t* counters;
     unsigned char* partials;
     uint32_t T, V, B, K, W;
-    uint32_t nq;          // 16-byte vectors per row in the stream-K space
-    uint32_t stride;      // partial slot bytes
-    uint32_t min_piece;   // minimum vectors per CTA
-    uint32_t stage_offsets;  // 1: copy off/out_off to shared memory
+    uint32_t nq;             // 16-byte vectors per row in the stream-K space
+    uint32_t stride;         // partial slot bytes
+    uint32_t min_piece;      // minimum vectors per warp
+    uint32_t stage_offsets;  // 1: copy off / out_off / echo to shared memory
 };
 
 // ---------------------------------------------------------------------------------
@@ -111,417 +134,422 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(const uint32_t* __restric
 }
 
 // ---------------------------------------------------------------------------------
-// Stream-K schedule over the vector space [0, R*nq): CTA c owns [start(c), start(c+1)).
-__device__ __forceinline__ uint64_t sk_start(uint64_t c, uint64_t Q, uint64_t G) { return c * Q / G; }
-// CTA that owns global vector g.
-__device__ __forceinline__ uint64_t sk_owner(uint64_t g, uint64_t Q, uint64_t G) {
-    return ((g + 1) * G - 1) / Q;
+// Stream-K schedule over the vector space [0, Q): warp g owns [start(g), start(g+1)).
+__device__ __forceinline__ uint64_t sk_start(uint64_t g, uint64_t Q, uint64_t G) { return g * Q / G; }
+// Warp that owns global vector v.
+__device__ __forceinline__ uint64_t sk_owner(uint64_t v, uint64_t Q, uint64_t G) {
+    return ((v + 1) * G - 1) / Q;
 }
 
-struct RowDesc {
-    uint32_t r;      // logits row
-    uint32_t t;      // target token
-    bool valid;
+// Per-lane running sum in the log2 domain.
+struct LaneSum {
+    float m;  // largest logit seen (-inf: none)
+    float c;  // reference, m * log2(e) rounded (0 while m is -inf)
+    float s;  // sum of 2^(x * log2(e) - c)
+    __device__ __forceinline__ void init() { m = neg_inf(); c = 0.f; s = 0.f; }
+    __device__ __forceinline__ void raise(float nm) {
+        const float nc = nm * kLog2e;
+        s = (s == 0.f) ? 0.f : s * ex2(c - nc);
+        c = nc;
+        m = nm;
+    }
+    __device__ __forceinline__ float term(float x) const { return ex2(fmaf(x, kLog2e, -c)); }
 };
 
-template <int SLOTS, bool TOPK>
-struct WarpTopK {
+template <int SLOTS>
+struct WarpList {
     float x[SLOTS];
     uint32_t id[SLOTS];
     __device__ __forceinline__ void reset() {
 #pragma unroll
         for (int k = 0; k < SLOTS; ++k) { x[k] = neg_inf(); id[k] = kPadId; }
     }
+    // K-th best value (slot K-1), broadcast to the warp.
+    __device__ __forceinline__ float kth(uint32_t K) const {
+        const uint32_t s = K - 1;
+        float v = x[0];
+        if constexpr (SLOTS == 2) v = (s >> 5) ? x[1] : x[0];
+        return __shfl_sync(kFull, v, s & 31);
+    }
+    // Merge one candidate per lane (32 in all, any order) into the list.
+    __device__ __forceinline__ void insert32(float cx, uint32_t ci, int lane) {
+        bitonic_sort32(cx, ci, lane);
+        float bx[SLOTS];
+        uint32_t bi[SLOTS];
+        bx[0] = cx;
+        bi[0] = ci;
+        if constexpr (SLOTS == 2) { bx[1] = neg_inf(); bi[1] = kPadId; }
+        merge_lists<SLOTS>(x, id, bx, bi, lane);
+    }
 };
 
-template <int SLOTS, bool TOPK, int U>
-struct alignas(16) RowsSmem {
-    float cand_x[kWarps][64];
-    uint32_t cand_i[kWarps][64];
-    float list_x[kWarps][32 * SLOTS];
-    uint32_t list_i[kWarps][32 * SLOTS];
-    float red_m[kWarps];
-    float red_s[kWarps];
-    uint32_t thr;
-    uint32_t last;
-    float xt;
-    uint32_t has_xt;
-};
-
+// Candidate buffer of one warp in shared memory (64 entries) + running threshold.
 template <int SLOTS>
-__device__ __forceinline__ float list_kth(const float (&x)[SLOTS], uint32_t K) {
-    const uint32_t s = K - 1;
-    float v = x[0];
-    if constexpr (SLOTS == 2) v = (s >> 5) ? x[1] : x[0];
-    return __shfl_sync(kFull, v, s & 31);
-}
+struct Selector {
+    WarpList<SLOTS> L;
+    float* cx;
+    uint32_t* ci;
+    float thr;
+    int cnt;
+    uint32_t K;
 
-// Flush 32 buffered candidates of this warp into its sorted list.
-template <int SLOTS>
-__device__ __forceinline__ void flush32(float (&lx)[SLOTS], uint32_t (&li)[SLOTS], float* cx, uint32_t* ci,
-                                        int cnt, int lane) {
-    __syncwarp();
-    float x = lane < cnt ? cx[lane] : neg_inf();
-    uint32_t id = lane < cnt ? ci[lane] : kPadId;
-    const bool more = lane + 32 < cnt;
-    float mx = 0.f;
-    uint32_t mi = 0;
-    if (more) { mx = cx[lane + 32]; mi = ci[lane + 32]; }
-    __syncwarp();
-    if (more) { cx[lane] = mx; ci[lane] = mi; }
-    __syncwarp();
-    bitonic_sort32(x, id, lane);
-    float bx[SLOTS];
-    uint32_t bi[SLOTS];
-    bx[0] = x; bi[0] = id;
-    if constexpr (SLOTS == 2) { bx[1] = neg_inf(); bi[1] = kPadId; }
-    merge_lists<SLOTS>(lx, li, bx, bi, lane);
-}
-
-// Load a stored partial's top-k into the lane-major list layout.
-template <int SLOTS>
-__device__ __forceinline__ void load_partial_list(const unsigned char* slot, uint32_t K, int lane,
-                                                  float (&x)[SLOTS], uint32_t (&id)[SLOTS]) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(slot);
-#pragma unroll
-    for (int k = 0; k < SLOTS; ++k) {
-        const uint32_t i = lane + 32 * k;
-        if (i < K) {
-            x[k] = __uint_as_float(__ldcg(w + 4 + i));
-            id[k] = __ldcg(w + 4 + K + i);
-        } else {
-            x[k] = neg_inf();
-            id[k] = kPadId;
+    __device__ __forceinline__ void init(float* bx, uint32_t* bi, uint32_t k) {
+        L.reset();
+        cx = bx;
+        ci = bi;
+        thr = neg_inf();
+        cnt = 0;
+        K = k;
+    }
+    __device__ __forceinline__ void flush(int lane) {
+        __syncwarp();
+        const float x = lane < cnt ? cx[lane] : neg_inf();
+        const uint32_t id = lane < cnt ? ci[lane] : kPadId;
+        const bool more = lane + 32 < cnt;
+        float mx = 0.f;
+        uint32_t mi = 0;
+        if (more) { mx = cx[lane + 32]; mi = ci[lane + 32]; }
+        __syncwarp();
+        if (more) { cx[lane] = mx; ci[lane] = mi; }
+        __syncwarp();
+        L.insert32(x, id, lane);
+        cnt = cnt > 32 ? cnt - 32 : 0;
+        thr = fmaxf(thr, L.kth(K));
+    }
+    // Append the elements of v flagged in pm (bit k: element k, id id0 + k).
+    // Warp-uniform call; the threshold may rise while appending.
+    __device__ __forceinline__ void append(const float4& v, uint32_t id0, uint32_t pm, int lane) {
+        unsigned any = __ballot_sync(kFull, pm != 0);
+        while (any) {
+            if (pm) {
+                const int k = __ffs(pm) - 1;
+                pm &= pm - 1;
+                const int slot = cnt + __popc(any & ((1u << lane) - 1u));
+                cx[slot] = pick(v, k);
+                ci[slot] = id0 + (uint32_t)k;
+            }
+            cnt += __popc(any);
+            if (cnt >= 32) {
+                flush(lane);
+                pm &= ge_mask(v, thr);
+            }
+            any = __ballot_sync(kFull, pm != 0);
         }
+    }
+};
+
+// Load one checked vector: elements outside [0, V) are -inf and masked out.
+__device__ __forceinline__ float4 load_checked(const float* rowp, const float* vbase, int64_t q, int a, uint32_t V,
+                                               uint32_t qf, uint32_t nfull, uint32_t& vm) {
+    if ((uint64_t)(q - qf) < nfull) {
+        vm = 0xFu;
+        return ldg_stream(vbase + 4 * q);
+    }
+    float t[4];
+    vm = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t e = 4 * q - a + k;
+        t[k] = neg_inf();
+        if (e >= 0 && e < (int64_t)V) { t[k] = rowp[e]; vm |= 1u << k; }
+    }
+    return make_float4(t[0], t[1], t[2], t[3]);
+}
+
+// Stream vectors [q0, q1) of one row: running sum per lane, top-k per warp.
+template <int SLOTS, bool TOPK, int U>
+__device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint32_t q0, uint32_t q1, int lane,
+                                             LaneSum& ls, Selector<SLOTS>& sel, bool t_here, uint32_t t,
+                                             float& xt) {
+    const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
+    const float* vbase = rowp - a;  // 16-byte aligned
+    const uint32_t qf = a ? 1u : 0u;
+    const uint32_t qe = (V + (uint32_t)a) >> 2;
+    const uint32_t nfull = qe > qf ? qe - qf : 0u;
+    const uint32_t qa = max(q0, qf), qb = min(q1, qe);
+    const uint32_t nblk = qb > qa ? (qb - qa) / (32u * U) : 0u;
+    const uint32_t bulk_lo = nblk ? qa : q0;
+    const uint32_t bulk_hi = nblk ? qa + nblk * 32u * U : q0;
+    bool xt_pending = t_here;
+
+    // ---- bulk: U full vectors per lane per block, no checks --------------------------
+    const float* vp = vbase + 4 * (size_t)(qa + lane);
+    uint32_t idb = 4u * (qa + (uint32_t)lane) - (uint32_t)a;
+    for (uint32_t blk = 0; blk < nblk; ++blk) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = ldg_stream(vp + 128 * u);
+        vp += 128 * U;
+        if (xt_pending) {  // the target id is known by now; its load overlaps the block
+            if (lane == 0) xt = rowp[t];
+            xt_pending = false;
+        }
+        float bm = max4(v[0]);
+#pragma unroll
+        for (int u = 1; u < U; ++u) bm = max3(bm, max3(v[u].x, v[u].y, v[u].z), v[u].w);
+        if (bm > ls.m) ls.raise(bm);
+        float acc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            acc[u] = (ls.term(v[u].x) + ls.term(v[u].y)) + (ls.term(v[u].z) + ls.term(v[u].w));
+#pragma unroll
+        for (int u = 1; u < U; ++u) acc[0] += acc[u];
+        ls.s += acc[0];
+
+        if constexpr (TOPK) {
+            if (blk == 0 && sel.cnt == 0 && sel.thr == neg_inf()) {
+                // Seed the list with each lane's best (and second best) element of this
+                // block, scanned in id order, so the threshold is useful at once.
+                float b1 = neg_inf(), b2 = neg_inf();
+                int p1 = -1, p2 = -1;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float x = pick(v[u], k);
+                        if (x > b1) {
+                            b2 = b1; p2 = p1;
+                            b1 = x; p1 = u * 4 + k;
+                        } else if (SLOTS == 2 && x > b2) {
+                            b2 = x; p2 = u * 4 + k;
+                        }
+                    }
+                }
+                const uint32_t i1 = p1 >= 0 ? idb + 128u * (uint32_t)(p1 >> 2) + (uint32_t)(p1 & 3) : kPadId;
+                sel.L.insert32(b1, i1, lane);
+                if constexpr (SLOTS == 2) {
+                    const uint32_t i2 = p2 >= 0 ? idb + 128u * (uint32_t)(p2 >> 2) + (uint32_t)(p2 & 3) : kPadId;
+                    sel.L.insert32(b2, i2, lane);
+                }
+                sel.thr = sel.L.kth(sel.K);
+                if (__any_sync(kFull, bm >= sel.thr)) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        uint32_t ex = 0;
+                        if ((p1 >> 2) == u) ex |= 1u << (p1 & 3);
+                        if (SLOTS == 2 && (p2 >> 2) == u) ex |= 1u << (p2 & 3);
+                        sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr) & ~ex, lane);
+                    }
+                }
+            } else if (__any_sync(kFull, bm >= sel.thr)) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr), lane);
+            }
+        }
+        idb += 128u * U;
+    }
+    if (xt_pending && lane == 0) xt = rowp[t];
+
+    // ---- edges: the partial first/last vectors and the tail, one checked vector per lane
+#pragma unroll 1
+    for (int part = 0; part < 2; ++part) {
+        const uint32_t lo = part ? bulk_hi : q0;
+        const uint32_t hi = part ? q1 : bulk_lo;
+        for (uint32_t qs = lo; qs < hi; qs += 32) {
+            const uint32_t q = qs + (uint32_t)lane;
+            float4 v = make_float4(neg_inf(), neg_inf(), neg_inf(), neg_inf());
+            uint32_t vm = 0;
+            if (q < hi) v = load_checked(rowp, vbase, q, a, V, qf, nfull, vm);
+            const float mx = max4(v);
+            if (mx > ls.m) ls.raise(mx);
+            ls.s += (ls.term(v.x) + ls.term(v.y)) + (ls.term(v.z) + ls.term(v.w));
+            if constexpr (TOPK) {
+                if (__any_sync(kFull, mx >= sel.thr))
+                    sel.append(v, 4u * q - (uint32_t)a, ge_mask(v, sel.thr) & vm, lane);
+            }
+        }
+    }
+    if constexpr (TOPK) {
+        if (sel.cnt > 0) sel.flush(lane);
+    }
+}
+
+// Write one finished row: K top columns and the target column.
+template <int SLOTS, bool TOPK>
+__device__ __forceinline__ void write_row(const RowsParams& p, uint32_t o, const WarpList<SLOTS>& L, float C,
+                                          float S, uint32_t t, bool has_xt, float xt, int lane) {
+    const double lse = (double)C * kLn2 + (double)logf(S);
+    const size_t ro = (size_t)o * p.W;
+    if constexpr (TOPK) {
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+            const uint32_t i = (uint32_t)lane + 32u * k;
+            if (i < p.K) {
+                p.out_lp[ro + i] = (float)((double)L.x[k] - lse);
+                p.out_tok[ro + i] = L.id[k];
+            }
+        }
+    }
+    if (lane == 0) {
+        float lpt = __int_as_float(0x7fc00000);
+        if (t < p.V && has_xt) lpt = (float)((double)xt - lse);
+        if (t >= p.V) atomicOr(p.status, kStatusTokenRange);
+        p.out_lp[ro + p.K] = lpt;
+        p.out_tok[ro + p.K] = t;
     }
 }
 
 template <int SLOTS, bool TOPK, int U>
-__global__ void __launch_bounds__(kThreads) k_rows(RowsParams p) {
+__global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) {
     extern __shared__ uint32_t s_dyn[];
-    __shared__ RowsSmem<SLOTS, TOPK, U> sm;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    __shared__ float s_cx[kWarps][64];
+    __shared__ uint32_t s_ci[kWarps][64];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t B = p.B, V = p.V, K = p.K;
 
     if (__ldcg(p.status) & kStatusOffsets) return;  // plan rejected the offsets
     const uint32_t R = __ldcg(p.out_off + B);
     if (R == 0) return;
     if (R > p.T) {
-        if (blockIdx.x == 0 && tid == 0) atomicOr(p.status, kStatusOffsets);
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusOffsets);
         return;
     }
     const uint64_t Q = (uint64_t)R * p.nq;
     uint64_t G = (Q + p.min_piece - 1) / p.min_piece;
-    if (G > gridDim.x) G = gridDim.x;
+    const uint64_t G_launch = (uint64_t)gridDim.x * kWarps;
+    if (G > G_launch) G = G_launch;
     if (G == 0) G = 1;
-    const uint64_t c = blockIdx.x;
-    if (c >= G) return;
+    if ((uint64_t)blockIdx.x * kWarps >= G) return;
 
     const uint32_t* off = p.off;
     const uint32_t* out_off = p.out_off;
+    const uint8_t* echo = p.echo;
     if (p.stage_offsets) {
-        for (uint32_t i = tid; i <= B; i += kThreads) {
+        for (uint32_t i = threadIdx.x; i <= B; i += kThreads) {
             s_dyn[i] = p.off[i];
             s_dyn[B + 1 + i] = p.out_off[i];
+            if (i < B) reinterpret_cast<uint8_t*>(s_dyn + 2 * (B + 1))[i] = p.echo[i];
         }
         __syncthreads();
         off = s_dyn;
         out_off = s_dyn + B + 1;
+        echo = reinterpret_cast<const uint8_t*>(s_dyn + 2 * (B + 1));
     }
+    // No CTA-wide barrier after this point: every warp runs on its own.
+    const uint64_t gw = (uint64_t)blockIdx.x * kWarps + w;
+    if (gw >= G) return;
 
-    const uint64_t g0 = sk_start(c, Q, G), g1 = sk_start(c + 1, Q, G);
+    const uint64_t g0 = sk_start(gw, Q, G), g1 = sk_start(gw + 1, Q, G);
     uint32_t o = (uint32_t)(g0 / p.nq);
     const uint32_t o_first = o;
     uint32_t q0 = (uint32_t)(g0 - (uint64_t)o * p.nq);
-    // batch of output row o: last b with out_off[b] <= o
-    uint32_t lo = 0, hi = B;  // answer in [lo, hi)
+    uint32_t lo = 0, hi = B;  // batch of row o: last b with out_off[b] <= o
     while (hi - lo > 1) {
-        uint32_t mid = (lo + hi) >> 1;
+        const uint32_t mid = (lo + hi) >> 1;
         if (out_off[mid] <= o) lo = mid; else hi = mid;
     }
     uint32_t b = lo;
-
-    float* cx = sm.cand_x[w];
-    uint32_t* ci = sm.cand_i[w];
 
     for (uint64_t g = g0; g < g1;) {
         const uint32_t q1 = (uint32_t)min((uint64_t)p.nq, (uint64_t)q0 + (g1 - g));
         const bool full = (q0 == 0) && (q1 == p.nq);
 
-        // ---- row descriptor -------------------------------------------------------
-        RowDesc d;
-        {
-            const uint32_t ob = out_off[b], oe = out_off[b + 1];
-            const uint32_t s = off[b], e = off[b + 1];
-            const uint32_t cnt = oe - ob;
-            const uint32_t len = e - s;
-            const bool echo_b = p.echo[b] != 0;
-            d.valid = (o >= ob) && (o < oe) && (e > s) && (e <= p.T) && (cnt == (echo_b ? len : 1u));
-            d.r = 0;
-            d.t = 0;
-            if (d.valid) {
-                d.r = e - cnt + (o - ob);
-                d.t = (d.r + 1 < e) ? p.tokens[d.r + 1] : p.sampled[b];
+        // ---- row descriptor (identical in every lane) ---------------------------------
+        const uint32_t ob = out_off[b], oe = out_off[b + 1];
+        const uint32_t sb = off[b], eb = off[b + 1];
+        const uint32_t cnt = oe - ob, len = eb - sb;
+        const bool valid = (o >= ob) && (o < oe) && (eb > sb) && (eb <= p.T) &&
+                           (cnt == (echo[b] ? len : 1u));
+        if (!valid) {
+            if (q0 == 0) {
+                for (uint32_t col = (uint32_t)lane; col < p.W; col += 32) {
+                    p.out_lp[(size_t)o * p.W + col] = __int_as_float(0x7fc00000);
+                    p.out_tok[(size_t)o * p.W + col] = kPadId;
+                }
             }
-        }
-
-        if (!d.valid) {
-            if (q0 == 0 && tid < (int)p.W) {
-                p.out_lp[(size_t)o * p.W + tid] = __int_as_float(0x7fc00000);
-                p.out_tok[(size_t)o * p.W + tid] = kPadId;
-            }
-            if (q0 == 0 && tid == 0) atomicOr(p.status, kStatusOffsets);
+            if (q0 == 0 && lane == 0) atomicOr(p.status, kStatusOffsets);
         } else {
-            const float* rowp = p.logits + (size_t)d.r * V;
+            const uint32_t r = eb - cnt + (o - ob);
+            const uint32_t t = (r + 1 < eb) ? p.tokens[r + 1] : p.sampled[b];
+            const float* rowp = p.logits + (size_t)r * V;
             const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
-            const float* vbase = rowp - a;  // 16-byte aligned
-            const uint32_t qf = a ? 1u : 0u;
-            const uint32_t qe = (V + (uint32_t)a) >> 2;
-            const uint32_t nfull = qe > qf ? qe - qf : 0u;
-
-            // target logit: the piece whose elements cover t loads it
             const int64_t e_lo = 4 * (int64_t)q0 - a, e_hi = 4 * (int64_t)q1 - a;
-            const bool t_here = d.t < V && (int64_t)d.t >= e_lo && (int64_t)d.t < e_hi;
+            const bool t_here = t < V && (int64_t)t >= e_lo && (int64_t)t < e_hi;
+
+            LaneSum ls;
+            ls.init();
+            Selector<SLOTS> sel;
+            sel.init(s_cx[w], s_ci[w], K);
             float xt = 0.f;
-            if (t_here && tid == 0) xt = rowp[d.t];
+            stream_piece<SLOTS, TOPK, U>(rowp, V, q0, q1, lane, ls, sel, t_here, t, xt);
 
-            float m = neg_inf(), ms = 0.f, s = 0.f;
-            float thr = neg_inf();
-            int cnt = 0;
-            WarpTopK<SLOTS, TOPK> L;
-            L.reset();
-            if (TOPK && tid == 0) sm.thr = f2ord(neg_inf());
-            if (TOPK) __syncthreads();
-
-            const uint32_t n = q1 - q0;
-            for (uint32_t base = 0; base < n; base += kThreads * U) {
-                float4 v[U];
-                uint32_t vm[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const uint32_t qi = base + u * kThreads + tid;
-                    const uint32_t q = q0 + qi;
-                    v[u] = make_float4(neg_inf(), neg_inf(), neg_inf(), neg_inf());
-                    vm[u] = 0;
-                    if (qi < n) {
-                        if (q - qf < nfull) {
-                            v[u] = ldg_stream(vbase + 4 * (size_t)q);
-                            vm[u] = 0xFu;
-                        } else {
-                            float t4[4];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const int64_t e = 4 * (int64_t)q - a + k;
-                                t4[k] = neg_inf();
-                                if (e >= 0 && e < (int64_t)V) { t4[k] = rowp[e]; vm[u] |= 1u << k; }
-                            }
-                            v[u] = make_float4(t4[0], t4[1], t4[2], t4[3]);
-                        }
-                    }
-                }
-                if (TOPK) thr = fmaxf(thr, ord2f(*(volatile uint32_t*)&sm.thr));
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const float4 x = v[u];
-                    const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-                    if (mx > m) {
-                        s *= ex2((m - mx) * kLog2e);
-                        m = mx;
-                        ms = mx;
-                    }
-                    s += ex2((x.x - ms) * kLog2e) + ex2((x.y - ms) * kLog2e) +
-                         ex2((x.z - ms) * kLog2e) + ex2((x.w - ms) * kLog2e);
-                    if constexpr (TOPK) {
-                        uint32_t pm = (mx >= thr) ? (ge_mask(x, thr) & vm[u]) : 0u;
-                        unsigned any = __ballot_sync(kFull, pm != 0);
-                        while (any) {
-                            if (pm) {
-                                const int k = __ffs(pm) - 1;
-                                pm &= pm - 1;
-                                const int slot = cnt + __popc(any & ((1u << lane) - 1u));
-                                cx[slot] = pick(x, k);
-                                ci[slot] = 4u * (q0 + base + u * kThreads + tid) - (uint32_t)a + (uint32_t)k;
-                            }
-                            cnt += __popc(any);
-                            if (cnt >= 32) {
-                                flush32<SLOTS>(L.x, L.id, cx, ci, cnt, lane);
-                                cnt -= 32;
-                                const float kth = list_kth<SLOTS>(L.x, K);
-                                if (lane == 0) atomicMax(&sm.thr, f2ord(kth));
-                                thr = fmaxf(thr, kth);
-                                pm &= ge_mask(x, thr);
-                            }
-                            any = __ballot_sync(kFull, pm != 0);
-                        }
-                    }
-                }
-            }
-            if constexpr (TOPK) {
-                if (cnt > 0) flush32<SLOTS>(L.x, L.id, cx, ci, cnt, lane);
-            }
-
-            // ---- CTA combine: (m, s) and the warps' lists -> warp 0 ----------------
-            warp_lse_reduce(m, s);
-            if (lane == 0) { sm.red_m[w] = m; sm.red_s[w] = s; }
-            if (tid == 0) { sm.xt = xt; sm.has_xt = t_here ? 1u : 0u; }
-            if constexpr (TOPK) {
-#pragma unroll
-                for (int k = 0; k < SLOTS; ++k) {
-                    sm.list_x[w][lane + 32 * k] = L.x[k];
-                    sm.list_i[w][lane + 32 * k] = L.id[k];
-                }
-            }
-            __syncthreads();
-            if constexpr (TOPK) {
-#pragma unroll
-                for (int st = 1; st < kWarps; st <<= 1) {
-                    if ((w & (2 * st - 1)) == 0) {
-                        float bx[SLOTS];
-                        uint32_t bi[SLOTS];
-#pragma unroll
-                        for (int k = 0; k < SLOTS; ++k) {
-                            bx[k] = sm.list_x[w + st][lane + 32 * k];
-                            bi[k] = sm.list_i[w + st][lane + 32 * k];
-                        }
-                        merge_lists<SLOTS>(L.x, L.id, bx, bi, lane);
-#pragma unroll
-                        for (int k = 0; k < SLOTS; ++k) {
-                            sm.list_x[w][lane + 32 * k] = L.x[k];
-                            sm.list_i[w][lane + 32 * k] = L.id[k];
-                        }
-                    }
-                    __syncthreads();
-                }
-            }
-            float M = neg_inf(), S = 0.f;
-            if (w == 0) {
-                M = lane < kWarps ? sm.red_m[lane] : neg_inf();
-                S = lane < kWarps ? sm.red_s[lane] : 0.f;
-                warp_lse_reduce(M, S);
-            }
+            float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, S = ls.s;
+            warp_lse2_reduce(C, S);
+            bool has_xt = t_here;
+            float xt_row = __shfl_sync(kFull, xt, 0);
 
             bool emit = full;
-            float xt_row = sm.xt;
-            bool has_xt_row = sm.has_xt != 0;
             if (!full) {
-                // ---- split row: publish this piece, the last arriving CTA merges -------
+                // ---- publish this piece; the warp taking the last ticket merges --------
                 const uint64_t gr = (uint64_t)o * p.nq;
-                const uint64_t c0 = sk_owner(gr, Q, G), c1 = sk_owner(gr + p.nq - 1, Q, G);
-                const uint32_t pieces = (uint32_t)(c1 - c0 + 1);
-                unsigned char* my_slot = p.partials + (size_t)(2 * c + (o == o_first ? 0 : 1)) * p.stride;
-                if (w == 0) {
-                    uint32_t* pw = reinterpret_cast<uint32_t*>(my_slot);
-                    if (lane == 0) {
-                        pw[0] = __float_as_uint(M);
-                        pw[1] = __float_as_uint(S);
-                        pw[2] = __float_as_uint(xt_row);
-                        pw[3] = has_xt_row ? 1u : 0u;
-                    }
-                    if constexpr (TOPK) {
-#pragma unroll
-                        for (int k = 0; k < SLOTS; ++k) {
-                            const uint32_t i = lane + 32 * k;
-                            if (i < K) { pw[4 + i] = __float_as_uint(L.x[k]); pw[4 + K + i] = L.id[k]; }
-                        }
-                    }
-                    __threadfence();
+                const uint64_t w0 = sk_owner(gr, Q, G), w1 = sk_owner(gr + p.nq - 1, Q, G);
+                const uint32_t pieces = (uint32_t)(w1 - w0 + 1);
+                uint32_t* pw = reinterpret_cast<uint32_t*>(p.partials +
+                                                           (size_t)(2 * gw + (o == o_first ? 0 : 1)) * p.stride);
+                if (lane == 0) {
+                    pw[0] = __float_as_uint(C);
+                    pw[1] = __float_as_uint(S);
+                    pw[2] = __float_as_uint(xt_row);
+                    pw[3] = has_xt ? 1u : 0u;
                 }
-                __syncthreads();
-                if (tid == 0) {
-                    __threadfence();
-                    const uint32_t ticket = atomicAdd(p.counters + c0, 1u);
-                    sm.last = (ticket == pieces - 1) ? 1u : 0u;
-                }
-                __syncthreads();
-                emit = sm.last != 0;
-                if (emit) {
-                    __threadfence();
-                    // warp w folds pieces w, w + kWarps, ...
-                    float pm_ = neg_inf(), ps_ = 0.f;
-                    L.reset();
-                    for (uint32_t j = w; j < pieces; j += kWarps) {
-                        const uint64_t cc = c0 + j;
-                        const uint32_t first_row = (uint32_t)(sk_start(cc, Q, G) / p.nq);
-                        const unsigned char* slot = p.partials + (size_t)(2 * cc + (o == first_row ? 0 : 1)) * p.stride;
-                        const uint32_t* pw = reinterpret_cast<const uint32_t*>(slot);
-                        if (lane == 0) {
-                            lse_combine(pm_, ps_, __uint_as_float(__ldcg(pw)), __uint_as_float(__ldcg(pw + 1)));
-                            if (__ldcg(pw + 3)) { sm.xt = __uint_as_float(__ldcg(pw + 2)); sm.has_xt = 1u; }
-                        }
-                        if constexpr (TOPK) {
-                            float bx[SLOTS];
-                            uint32_t bi[SLOTS];
-                            load_partial_list<SLOTS>(slot, K, lane, bx, bi);
-                            merge_lists<SLOTS>(L.x, L.id, bx, bi, lane);
-                        }
-                    }
-                    if (lane == 0) { sm.red_m[w] = pm_; sm.red_s[w] = ps_; }
-                    if constexpr (TOPK) {
-#pragma unroll
-                        for (int k = 0; k < SLOTS; ++k) {
-                            sm.list_x[w][lane + 32 * k] = L.x[k];
-                            sm.list_i[w][lane + 32 * k] = L.id[k];
-                        }
-                    }
-                    __syncthreads();
-                    if constexpr (TOPK) {
-#pragma unroll
-                        for (int st = 1; st < kWarps; st <<= 1) {
-                            if ((w & (2 * st - 1)) == 0) {
-                                float bx[SLOTS];
-                                uint32_t bi[SLOTS];
-#pragma unroll
-                                for (int k = 0; k < SLOTS; ++k) {
-                                    bx[k] = sm.list_x[w + st][lane + 32 * k];
-                                    bi[k] = sm.list_i[w + st][lane + 32 * k];
-                                }
-                                merge_lists<SLOTS>(L.x, L.id, bx, bi, lane);
-#pragma unroll
-                                for (int k = 0; k < SLOTS; ++k) {
-                                    sm.list_x[w][lane + 32 * k] = L.x[k];
-                                    sm.list_i[w][lane + 32 * k] = L.id[k];
-                                }
-                            }
-                            __syncthreads();
-                        }
-                    }
-                    if (w == 0) {
-                        M = lane < kWarps ? sm.red_m[lane] : neg_inf();
-                        S = lane < kWarps ? sm.red_s[lane] : 0.f;
-                        warp_lse_reduce(M, S);
-                    }
-                    xt_row = sm.xt;
-                    has_xt_row = sm.has_xt != 0;
-                    if (tid == 0) p.counters[c0] = 0u;  // ready for the next call
-                }
-            }
-
-            // ---- write the row: K top columns + the target column -----------------
-            if (emit && w == 0) {
-                const double lse = (double)M + (double)logf(S);
-                const size_t ro = (size_t)o * p.W;
                 if constexpr (TOPK) {
 #pragma unroll
                     for (int k = 0; k < SLOTS; ++k) {
-                        const uint32_t i = lane + 32 * k;
-                        if (i < K) {
-                            p.out_lp[ro + i] = (float)((double)L.x[k] - lse);
-                            p.out_tok[ro + i] = L.id[k];
-                        }
+                        const uint32_t i = (uint32_t)lane + 32u * k;
+                        if (i < K) { pw[4 + i] = __float_as_uint(sel.L.x[k]); pw[4 + K + i] = sel.L.id[k]; }
                     }
                 }
-                if (lane == 0) {
-                    float lpt = __int_as_float(0x7fc00000);
-                    if (d.t < V && has_xt_row) lpt = (float)((double)xt_row - lse);
-                    if (d.t >= V) atomicOr(p.status, kStatusTokenRange);
-                    p.out_lp[ro + K] = lpt;
-                    p.out_tok[ro + K] = d.t;
+                __threadfence();
+                __syncwarp();
+                uint32_t ticket = 0;
+                if (lane == 0) ticket = atomicAdd(p.counters + w0, 1u);
+                ticket = __shfl_sync(kFull, ticket, 0);
+                emit = (ticket == pieces - 1);
+                if (emit) {
+                    __threadfence();
+                    // headers: lane j folds pieces j, j+32, ...
+                    C = neg_inf();
+                    S = 0.f;
+                    has_xt = false;
+                    for (uint32_t j = (uint32_t)lane; j < pieces; j += 32) {
+                        const uint64_t wj = w0 + j;
+                        const uint32_t first_row = (uint32_t)(sk_start(wj, Q, G) / p.nq);
+                        const uint32_t* hw = reinterpret_cast<const uint32_t*>(
+                            p.partials + (size_t)(2 * wj + (o == first_row ? 0 : 1)) * p.stride);
+                        lse2_combine(C, S, __uint_as_float(__ldcg(hw)), __uint_as_float(__ldcg(hw + 1)));
+                        if (__ldcg(hw + 3)) { xt_row = __uint_as_float(__ldcg(hw + 2)); has_xt = true; }
+                    }
+                    warp_lse2_reduce(C, S);
+                    const unsigned hx = __ballot_sync(kFull, has_xt);
+                    has_xt = hx != 0;
+                    xt_row = __shfl_sync(kFull, xt_row, hx ? __ffs(hx) - 1 : 0);
+                    if constexpr (TOPK) {
+                        // top-k lists: all pieces' entries as candidates, 32 per insert
+                        sel.L.reset();
+                        const uint32_t total = pieces * K;
+                        for (uint32_t e0 = 0; e0 < total; e0 += 32) {
+                            const uint32_t e = e0 + (uint32_t)lane;
+                            float x = neg_inf();
+                            uint32_t id = kPadId;
+                            if (e < total) {
+                                const uint32_t j = e / K, rk = e - j * K;
+                                const uint64_t wj = w0 + j;
+                                const uint32_t first_row = (uint32_t)(sk_start(wj, Q, G) / p.nq);
+                                const uint32_t* lw = reinterpret_cast<const uint32_t*>(
+                                    p.partials + (size_t)(2 * wj + (o == first_row ? 0 : 1)) * p.stride);
+                                x = __uint_as_float(__ldcg(lw + 4 + rk));
+                                id = __ldcg(lw + 4 + K + rk);
+                            }
+                            sel.L.insert32(x, id, lane);
+                        }
+                    }
+                    if (lane == 0) p.counters[w0] = 0u;  // ready for the next call
                 }
             }
+            if (emit) write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, has_xt, xt_row, lane);
         }
-        __syncthreads();
 
-        // ---- next piece -------------------------------------------------------------
+        // ---- next piece -----------------------------------------------------------
         g += q1 - q0;
         q0 = 0;
         ++o;

@@ -14,10 +14,10 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr uint32_t kMaxCtasPerSm = 8;
-constexpr uint32_t kMinPieceVec = 2048;         // 32 KB of logits per CTA at least
+constexpr uint32_t kMaxCtasPerSm = 4;           // launch cap; sizes the workspace
+constexpr uint32_t kMinPieceVec = 1024;         // 16 KB of logits per warp at least
 constexpr uint32_t kStageOffsetsMax = 2048;     // stage off/out_off in smem when B+1 <= this
-constexpr uint32_t kUnroll = 4;
+constexpr uint32_t kUnroll = LP_UNROLL;
 constexpr int kVariants = 3;                    // levels 0 | 1..5 | 6
 
 struct DeviceInfo {
@@ -73,10 +73,13 @@ int occupancy(DeviceInfo* d, int v, size_t smem) {
 
 size_t counters_bytes(uint32_t g_max) { return ((size_t)g_max * 4 + 255) & ~(size_t)255; }
 
+// Largest number of warps a launch can have on a device with `sms` SMs.
+uint32_t max_warps(int sms) { return (uint32_t)sms * kMaxCtasPerSm * lpk::kWarps; }
+
 size_t workspace_bytes_for(int sms, uint32_t levels) {
     const uint32_t K = (1u << levels) - 1u;
-    const uint32_t g_max = (uint32_t)sms * kMaxCtasPerSm;
-    return sizeof(lpk::WsHeader) + counters_bytes(g_max) + (size_t)2 * g_max * lpk::partial_stride_bytes(K);
+    const uint32_t nw = max_warps(sms);
+    return sizeof(lpk::WsHeader) + counters_bytes(nw) + (size_t)2 * nw * lpk::partial_stride_bytes(K);
 }
 
 }  // namespace
@@ -102,7 +105,7 @@ lp_status lp_ragged_plan(const uint32_t* logit_row_offsets, const uint8_t* echo,
     int dev;
     DeviceInfo* d;
     if (!device_info(&dev, &d)) return LP_ERR_CUDA;
-    const uint32_t g_max = (uint32_t)d->sms * kMaxCtasPerSm;
+    const uint32_t g_max = max_warps(d->sms);
     if (workspace_bytes < sizeof(lpk::WsHeader) + counters_bytes(g_max)) return LP_ERR_WORKSPACE;
     auto* hdr = static_cast<lpk::WsHeader*>(workspace);
     auto* counters = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) + sizeof(lpk::WsHeader));
@@ -139,7 +142,7 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
 
     const uint32_t K = (1u << levels) - 1u;
     const uint32_t W = levels ? (1u << levels) : 1u;
-    const uint32_t g_max = (uint32_t)d->sms * kMaxCtasPerSm;
+    const uint32_t g_max = max_warps(d->sms);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
 
     lpk::RowsParams p;
@@ -164,12 +167,11 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
     p.stride = lpk::partial_stride_bytes(K);
     p.min_piece = kMinPieceVec;
     p.stage_offsets = (B + 1u <= kStageOffsetsMax) ? 1u : 0u;
-    const size_t smem = p.stage_offsets ? (size_t)2 * (B + 1u) * sizeof(uint32_t) : 0;
+    const size_t smem = p.stage_offsets ? (size_t)2 * (B + 1u) * sizeof(uint32_t) + ((B + 3u) & ~3u) : 0;
 
     const int v = variant_of(levels);
     const int occ = occupancy(d, v, smem);
-    uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;
-    if (grid > g_max) grid = g_max;
+    const uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;  // occ <= kMaxCtasPerSm
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (v) {
         case 0: lpk::k_rows<1, false, kUnroll><<<grid, lpk::kThreads, smem, s>>>(p); break;
@@ -258,7 +260,7 @@ extern "C" lp_status lp_ragged_compute_noalloc(const float* logits, uint32_t T, 
     if (!noalloc_scratch(dev, &scratch)) return LP_ERR_CUDA;
     // The array keeps the previous call's contents: zero the status word and the
     // arrival counters (the partial tuples are always written before they are read).
-    const uint32_t g_max = (uint32_t)d->sms * kMaxCtasPerSm;
+    const uint32_t g_max = max_warps(d->sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(scratch, 0, sizeof(lpk::WsHeader) + counters_bytes(g_max), s) != cudaSuccess) {
         (void)cudaGetLastError();

@@ -2,7 +2,9 @@
 same inputs, compare element by element.
 
 Tolerance: token ids and row layout bit-exact; logprobs |delta| <= 1e-4 absolute
-(NaN where the oracle has NaN, -inf where it has -inf)."""
+(NaN where the oracle has NaN, -inf where it has -inf). Where |logprob| >= 1024 the
+fp32 output itself cannot resolve 1e-4 (its spacing there is >= 1.2e-4), so the bound
+is one fp32 spacing at the reference value instead."""
 
 from __future__ import annotations
 
@@ -61,9 +63,10 @@ def compare(gpu_lp, gpu_tok, ref_lp, ref_tok, what=""):
     assert np.all(gpu_lp[inf_ref] == ref32[inf_ref]), f"{what}: inf signs differ"
     fin = ~(nan_ref | inf_ref)
     err = np.abs(gpu_lp[fin].astype(np.float64) - ref32[fin])
+    tol = np.maximum(ATOL, np.spacing(np.abs(ref32[fin]).astype(np.float32)).astype(np.float64))
     if err.size:
-        i = int(np.argmax(err))
-        assert err[i] <= ATOL, f"{what}: max |delta| {err[i]:.3g} > {ATOL}"
+        i = int(np.argmax(err - tol))
+        assert err[i] <= tol[i], f"{what}: |delta| {err[i]:.3g} > {tol[i]:.3g} at reference {ref32[fin][i]:.6g}"
     return float(err.max()) if err.size else 0.0
 
 
