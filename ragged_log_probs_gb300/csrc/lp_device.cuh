@@ -31,6 +31,18 @@ __device__ __forceinline__ float4 ldg_stream(const float* p) {
     return v;
 }
 
+// Asynchronous 16-byte global -> shared copy (L1 bypass, 256-byte L2 prefetch) and
+// its group bookkeeping. wait_group N returns once at most N of this thread's most
+// recent groups are still in flight (a hardware wait, no polling loop).
+__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const float* gptr) {
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(smem_addr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ bool better(float xa, uint32_t ia, float xb, uint32_t ib) {
     return xa > xb || (xa == xb && ia < ib);
 }
@@ -115,6 +127,26 @@ __device__ __forceinline__ void merge_lists(float (&ax)[SLOTS], uint32_t (&ai)[S
         ax[0] = c0x; ai[0] = c0i;
         ax[1] = c1x; ai[1] = c1i;
     }
+}
+
+// Packed fp32 pair arithmetic (one instruction for two lanes of data, sm_100+).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.ftz.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.ftz.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
 
 // max(a, b, c) in one instruction (three-source max, sm_100+).

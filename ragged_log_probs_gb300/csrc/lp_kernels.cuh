@@ -37,6 +37,10 @@ namespace lpk {
 #ifndef LP_MIN_BLOCKS
 #define LP_MIN_BLOCKS 3
 #endif
+#ifndef LP_STAGES
+#define LP_STAGES 4  // blocks per warp in the shared-memory ring (power of two)
+#endif
+
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
@@ -45,7 +49,8 @@ constexpr uint32_t kStatusOffsets = 1u << 4;     // bit of LP_ERR_OFFSETS
 constexpr uint32_t kStatusTokenRange = 1u << 5;  // bit of LP_ERR_TOKEN_RANGE
 constexpr double kLn2 = 0.69314718055994530942;
 
-// Workspace: [header 256 B][counters u32 x max warps, padded to 256 B][partial slots].
+// Workspace: [header 256 B][arrival counters u32 x max warps, zeroed by plan, padded
+// to 256 B][partial slots].
 struct WsHeader {
     uint32_t status;
     uint32_t rows;
@@ -69,7 +74,7 @@ struct RowsParams {
     float* out_lp;
     uint32_t* out_tok;
     uint32_t* status;
-    uint32_t* counters;
+    uint32_t* counters;      // per split row (indexed by its first warp): pieces arrived
     unsigned char* partials;
     uint32_t T, V, B, K, W;
     uint32_t nq;             // 16-byte vectors per row in the stream-K space
@@ -153,7 +158,13 @@ struct LaneSum {
         c = nc;
         m = nm;
     }
-    __device__ __forceinline__ float term(float x) const { return ex2(fmaf(x, kLog2e, -c)); }
+    // Terms of four logits: two packed FMAs, four EX2, one packed add.
+    __device__ __forceinline__ float2 term4(const float4& v) const {
+        const float2 l2e = make_float2(kLog2e, kLog2e), mc = make_float2(-c, -c);
+        const float2 y0 = ffma2(make_float2(v.x, v.y), l2e, mc);
+        const float2 y1 = ffma2(make_float2(v.z, v.w), l2e, mc);
+        return fadd2(make_float2(ex2(y0.x), ex2(y0.y)), make_float2(ex2(y1.x), ex2(y1.y)));
+    }
 };
 
 template <int SLOTS>
@@ -164,7 +175,7 @@ struct WarpList {
 #pragma unroll
         for (int k = 0; k < SLOTS; ++k) { x[k] = neg_inf(); id[k] = kPadId; }
     }
-    // K-th best value (slot K-1), broadcast to the warp.
+    // Value of entry K-1, broadcast to the warp.
     __device__ __forceinline__ float kth(uint32_t K) const {
         const uint32_t s = K - 1;
         float v = x[0];
@@ -183,7 +194,10 @@ struct WarpList {
     }
 };
 
-// Candidate buffer of one warp in shared memory (64 entries) + running threshold.
+// Top-k selection state of one warp: sorted list in registers, a 64-entry candidate
+// buffer in shared memory, and the filter threshold thr = the list's K-th value. An
+// element below thr cannot enter the top-k (K better elements are already known), so
+// only elements >= thr are buffered; a full buffer is sorted into the list.
 template <int SLOTS>
 struct Selector {
     WarpList<SLOTS> L;
@@ -257,10 +271,13 @@ __device__ __forceinline__ float4 load_checked(const float* rowp, const float* v
 }
 
 // Stream vectors [q0, q1) of one row: running sum per lane, top-k per warp.
-template <int SLOTS, bool TOPK, int U>
+// Full blocks (U vectors per lane, 512*U contiguous bytes per warp) go through a ring
+// of STAGES blocks in shared memory filled by cp.async, so STAGES-1 blocks stay in
+// flight while one is reduced; each lane reads back only what it copied itself.
+template <int SLOTS, bool TOPK, int U, int STAGES>
 __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint32_t q0, uint32_t q1, int lane,
                                              LaneSum& ls, Selector<SLOTS>& sel, bool t_here, uint32_t t,
-                                             float& xt) {
+                                             float& xt, float4* ring) {
     const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
     const float* vbase = rowp - a;  // 16-byte aligned
     const uint32_t qf = a ? 1u : 0u;
@@ -274,27 +291,44 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
 
     // ---- bulk: U full vectors per lane per block, no checks --------------------------
     const float* vp = vbase + 4 * (size_t)(qa + lane);
+    const uint32_t ring_lane = (uint32_t)__cvta_generic_to_shared(ring + lane);
+    auto issue = [&](uint32_t blk) {
+        if (blk < nblk) {
+            const float* src = vp + (size_t)blk * 128u * U;
+            const uint32_t dst = ring_lane + (blk & (STAGES - 1)) * (U * 512u);
+#pragma unroll
+            for (int u = 0; u < U; ++u) cp_async16(dst + 512u * u, src + 128 * u);
+        }
+        cp_async_commit();
+    };
+    if (nblk) {
+#pragma unroll
+        for (int s0 = 0; s0 < STAGES - 1; ++s0) issue((uint32_t)s0);
+    }
     uint32_t idb = 4u * (qa + (uint32_t)lane) - (uint32_t)a;
     for (uint32_t blk = 0; blk < nblk; ++blk) {
+        issue(blk + STAGES - 1);
+        cp_async_wait<STAGES - 1>();
         float4 v[U];
+        const float4* stage = ring + (blk & (STAGES - 1)) * (U * 32u) + lane;
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = ldg_stream(vp + 128 * u);
-        vp += 128 * U;
-        if (xt_pending) {  // the target id is known by now; its load overlaps the block
+        for (int u = 0; u < U; ++u) v[u] = stage[32 * u];
+        if (xt_pending) {  // the target id has arrived by now
             if (lane == 0) xt = rowp[t];
             xt_pending = false;
         }
-        float bm = max4(v[0]);
+        float mu[U];
 #pragma unroll
-        for (int u = 1; u < U; ++u) bm = max3(bm, max3(v[u].x, v[u].y, v[u].z), v[u].w);
+        for (int u = 0; u < U; ++u) mu[u] = max4(v[u]);
+        float bm = mu[0];
+#pragma unroll
+        for (int u = 1; u + 1 < U; u += 2) bm = max3(bm, mu[u], mu[u + 1]);
+        if ((U & 1) == 0) bm = fmaxf(bm, mu[U - 1]);
         if (bm > ls.m) ls.raise(bm);
-        float acc[U];
+        float2 acc = ls.term4(v[0]);
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            acc[u] = (ls.term(v[u].x) + ls.term(v[u].y)) + (ls.term(v[u].z) + ls.term(v[u].w));
-#pragma unroll
-        for (int u = 1; u < U; ++u) acc[0] += acc[u];
-        ls.s += acc[0];
+        for (int u = 1; u < U; ++u) acc = fadd2(acc, ls.term4(v[u]));
+        ls.s += acc.x + acc.y;
 
         if constexpr (TOPK) {
             if (blk == 0 && sel.cnt == 0 && sel.thr == neg_inf()) {
@@ -325,7 +359,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
                 if (__any_sync(kFull, bm >= sel.thr)) {
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        uint32_t ex = 0;
+                        uint32_t ex = 0;  // the seeded elements are already in the list
                         if ((p1 >> 2) == u) ex |= 1u << (p1 & 3);
                         if (SLOTS == 2 && (p2 >> 2) == u) ex |= 1u << (p2 & 3);
                         sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr) & ~ex, lane);
@@ -352,7 +386,8 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
             if (q < hi) v = load_checked(rowp, vbase, q, a, V, qf, nfull, vm);
             const float mx = max4(v);
             if (mx > ls.m) ls.raise(mx);
-            ls.s += (ls.term(v.x) + ls.term(v.y)) + (ls.term(v.z) + ls.term(v.w));
+            const float2 tt = ls.term4(v);
+            ls.s += tt.x + tt.y;
             if constexpr (TOPK) {
                 if (__any_sync(kFull, mx >= sel.thr))
                     sel.append(v, 4u * q - (uint32_t)a, ge_mask(v, sel.thr) & vm, lane);
@@ -389,16 +424,130 @@ __device__ __forceinline__ void write_row(const RowsParams& p, uint32_t o, const
     }
 }
 
-template <int SLOTS, bool TOPK, int U>
+// Partial tuple of piece j of a row whose first piece belongs to warp w0. A warp
+// stores the piece of its first row in slot 0 and that of its last row in slot 1;
+// only piece 0 can be its warp's last row.
+__device__ __forceinline__ uint32_t* piece_slot(const RowsParams& p, uint64_t w0, uint32_t j, bool tail0) {
+    return reinterpret_cast<uint32_t*>(p.partials + (size_t)(2 * (w0 + j) + ((j == 0 && tail0) ? 1 : 0)) * p.stride);
+}
+
+template <int SLOTS, bool TOPK>
+__device__ __forceinline__ void store_piece(uint32_t* pw, uint32_t K, const WarpList<SLOTS>& L, float C, float S,
+                                            bool has_xt, float xt, int lane) {
+    if (lane == 0) {
+        pw[0] = __float_as_uint(C);
+        pw[1] = __float_as_uint(S);
+        pw[2] = __float_as_uint(xt);
+        pw[3] = has_xt ? 1u : 0u;
+    }
+    if constexpr (TOPK) {
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+            const uint32_t i = (uint32_t)lane + 32u * k;
+            if (i < K) { pw[4 + i] = __float_as_uint(L.x[k]); pw[4 + K + i] = L.id[k]; }
+        }
+    }
+}
+
+template <int SLOTS>
+__device__ __forceinline__ void load_piece_list(const uint32_t* pw, uint32_t K, int lane, float (&x)[SLOTS],
+                                                uint32_t (&id)[SLOTS]) {
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) {
+        const uint32_t i = (uint32_t)lane + 32u * k;
+        x[k] = neg_inf();
+        id[k] = kPadId;
+        if (i < K) {
+            x[k] = __uint_as_float(__ldcg(pw + 4 + i));
+            id[k] = __ldcg(pw + 4 + K + i);
+        }
+    }
+}
+
+// Merge all pieces of a split row (called by the warp that took the last ticket):
+// (reference, sum) and the target logit from the headers, the top-k by sequential
+// bitonic merges of the pieces' sorted lists (next list prefetched).
+template <int SLOTS, bool TOPK>
+__device__ __forceinline__ void merge_pieces(const RowsParams& p, uint64_t w0, uint32_t pieces, bool tail0, int lane,
+                                             WarpList<SLOTS>& L, float& C, float& S, bool& has_xt, float& xt) {
+    C = neg_inf();
+    S = 0.f;
+    has_xt = false;
+    xt = 0.f;
+    for (uint32_t j = (uint32_t)lane; j < pieces; j += 32) {
+        const uint32_t* hw = piece_slot(p, w0, j, tail0);
+        const float hc = __uint_as_float(__ldcg(hw)), hs = __uint_as_float(__ldcg(hw + 1));
+        const float hx = __uint_as_float(__ldcg(hw + 2));
+        const uint32_t hh = __ldcg(hw + 3);
+        lse2_combine(C, S, hc, hs);
+        if (hh) { xt = hx; has_xt = true; }
+    }
+    L.reset();
+    if constexpr (TOPK) {
+        float nx[SLOTS];
+        uint32_t ni[SLOTS];
+        load_piece_list<SLOTS>(piece_slot(p, w0, 0, tail0), p.K, lane, nx, ni);
+        for (uint32_t j = 0; j < pieces; ++j) {
+            float cx[SLOTS];
+            uint32_t ci[SLOTS];
+#pragma unroll
+            for (int k = 0; k < SLOTS; ++k) { cx[k] = nx[k]; ci[k] = ni[k]; }
+            if (j + 1 < pieces) load_piece_list<SLOTS>(piece_slot(p, w0, j + 1, tail0), p.K, lane, nx, ni);
+            merge_lists<SLOTS>(L.x, L.id, cx, ci, lane);
+        }
+    }
+    warp_lse2_reduce(C, S);
+    const unsigned hb = __ballot_sync(kFull, has_xt);
+    has_xt = hb != 0;
+    xt = __shfl_sync(kFull, xt, hb ? __ffs(hb) - 1 : 0);
+}
+
+// Publish a piece and take a ticket; true for the warp that arrives last.
+__device__ __forceinline__ bool take_ticket(const RowsParams& p, uint64_t w0, uint32_t pieces, int lane) {
+    __threadfence();
+    __syncwarp();
+    uint32_t ticket = 0;
+    if (lane == 0) ticket = atomicAdd(p.counters + w0, 1u);
+    ticket = __shfl_sync(kFull, ticket, 0);
+    const bool last = ticket == pieces - 1;
+    if (last) __threadfence();
+    return last;
+}
+
+// Dynamic shared memory: the warps' rings, then the staged offsets.
+template <int U, int STAGES>
+__host__ __device__ constexpr uint32_t ring_bytes() { return (uint32_t)kWarps * STAGES * U * 512u; }
+
+template <int SLOTS, bool TOPK, int U, int STAGES>
 __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) {
-    extern __shared__ uint32_t s_dyn[];
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    float4* rings = reinterpret_cast<float4*>(s_raw);
+    uint32_t* s_dyn = reinterpret_cast<uint32_t*>(s_raw + ring_bytes<U, STAGES>());
     __shared__ float s_cx[kWarps][64];
     __shared__ uint32_t s_ci[kWarps][64];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t B = p.B, V = p.V, K = p.K;
 
-    if (__ldcg(p.status) & kStatusOffsets) return;  // plan rejected the offsets
+    // Status, row count and the offsets are fetched in one round trip.
+    const uint32_t status = __ldcg(p.status);
     const uint32_t R = __ldcg(p.out_off + B);
+    const uint32_t* off = p.off;
+    const uint32_t* out_off = p.out_off;
+    const uint8_t* echo = p.echo;
+    if (p.stage_offsets) {
+        for (uint32_t i = threadIdx.x; i <= B; i += kThreads) {
+            const uint32_t a0 = p.off[i], a1 = p.out_off[i];
+            const uint8_t e = i < B ? p.echo[i] : 0;
+            s_dyn[i] = a0;
+            s_dyn[B + 1 + i] = a1;
+            if (i < B) reinterpret_cast<uint8_t*>(s_dyn + 2 * (B + 1))[i] = e;
+        }
+        off = s_dyn;
+        out_off = s_dyn + B + 1;
+        echo = reinterpret_cast<const uint8_t*>(s_dyn + 2 * (B + 1));
+        __syncthreads();
+    }
+    if (status & kStatusOffsets) return;  // plan rejected the offsets
     if (R == 0) return;
     if (R > p.T) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusOffsets);
@@ -409,22 +558,6 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
     const uint64_t G_launch = (uint64_t)gridDim.x * kWarps;
     if (G > G_launch) G = G_launch;
     if (G == 0) G = 1;
-    if ((uint64_t)blockIdx.x * kWarps >= G) return;
-
-    const uint32_t* off = p.off;
-    const uint32_t* out_off = p.out_off;
-    const uint8_t* echo = p.echo;
-    if (p.stage_offsets) {
-        for (uint32_t i = threadIdx.x; i <= B; i += kThreads) {
-            s_dyn[i] = p.off[i];
-            s_dyn[B + 1 + i] = p.out_off[i];
-            if (i < B) reinterpret_cast<uint8_t*>(s_dyn + 2 * (B + 1))[i] = p.echo[i];
-        }
-        __syncthreads();
-        off = s_dyn;
-        out_off = s_dyn + B + 1;
-        echo = reinterpret_cast<const uint8_t*>(s_dyn + 2 * (B + 1));
-    }
     // No CTA-wide barrier after this point: every warp runs on its own.
     const uint64_t gw = (uint64_t)blockIdx.x * kWarps + w;
     if (gw >= G) return;
@@ -439,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
         if (out_off[mid] <= o) lo = mid; else hi = mid;
     }
     uint32_t b = lo;
+    float4* ring = rings + (size_t)w * STAGES * U * 32;
 
     for (uint64_t g = g0; g < g1;) {
         const uint32_t q1 = (uint32_t)min((uint64_t)p.nq, (uint64_t)q0 + (g1 - g));
@@ -471,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
             Selector<SLOTS> sel;
             sel.init(s_cx[w], s_ci[w], K);
             float xt = 0.f;
-            stream_piece<SLOTS, TOPK, U>(rowp, V, q0, q1, lane, ls, sel, t_here, t, xt);
+            stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, q0, q1, lane, ls, sel, t_here, t, xt, ring);
 
             float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, S = ls.s;
             warp_lse2_reduce(C, S);
@@ -484,65 +618,13 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
                 const uint64_t gr = (uint64_t)o * p.nq;
                 const uint64_t w0 = sk_owner(gr, Q, G), w1 = sk_owner(gr + p.nq - 1, Q, G);
                 const uint32_t pieces = (uint32_t)(w1 - w0 + 1);
-                uint32_t* pw = reinterpret_cast<uint32_t*>(p.partials +
-                                                           (size_t)(2 * gw + (o == o_first ? 0 : 1)) * p.stride);
-                if (lane == 0) {
-                    pw[0] = __float_as_uint(C);
-                    pw[1] = __float_as_uint(S);
-                    pw[2] = __float_as_uint(xt_row);
-                    pw[3] = has_xt ? 1u : 0u;
-                }
-                if constexpr (TOPK) {
-#pragma unroll
-                    for (int k = 0; k < SLOTS; ++k) {
-                        const uint32_t i = (uint32_t)lane + 32u * k;
-                        if (i < K) { pw[4 + i] = __float_as_uint(sel.L.x[k]); pw[4 + K + i] = sel.L.id[k]; }
-                    }
-                }
-                __threadfence();
-                __syncwarp();
-                uint32_t ticket = 0;
-                if (lane == 0) ticket = atomicAdd(p.counters + w0, 1u);
-                ticket = __shfl_sync(kFull, ticket, 0);
-                emit = (ticket == pieces - 1);
+                store_piece<SLOTS, TOPK>(reinterpret_cast<uint32_t*>(
+                                             p.partials + (size_t)(2 * gw + (o == o_first ? 0 : 1)) * p.stride),
+                                         K, sel.L, C, S, has_xt, xt_row, lane);
+                emit = take_ticket(p, w0, pieces, lane);
                 if (emit) {
-                    __threadfence();
-                    // headers: lane j folds pieces j, j+32, ...
-                    C = neg_inf();
-                    S = 0.f;
-                    has_xt = false;
-                    for (uint32_t j = (uint32_t)lane; j < pieces; j += 32) {
-                        const uint64_t wj = w0 + j;
-                        const uint32_t first_row = (uint32_t)(sk_start(wj, Q, G) / p.nq);
-                        const uint32_t* hw = reinterpret_cast<const uint32_t*>(
-                            p.partials + (size_t)(2 * wj + (o == first_row ? 0 : 1)) * p.stride);
-                        lse2_combine(C, S, __uint_as_float(__ldcg(hw)), __uint_as_float(__ldcg(hw + 1)));
-                        if (__ldcg(hw + 3)) { xt_row = __uint_as_float(__ldcg(hw + 2)); has_xt = true; }
-                    }
-                    warp_lse2_reduce(C, S);
-                    const unsigned hx = __ballot_sync(kFull, has_xt);
-                    has_xt = hx != 0;
-                    xt_row = __shfl_sync(kFull, xt_row, hx ? __ffs(hx) - 1 : 0);
-                    if constexpr (TOPK) {
-                        // top-k lists: all pieces' entries as candidates, 32 per insert
-                        sel.L.reset();
-                        const uint32_t total = pieces * K;
-                        for (uint32_t e0 = 0; e0 < total; e0 += 32) {
-                            const uint32_t e = e0 + (uint32_t)lane;
-                            float x = neg_inf();
-                            uint32_t id = kPadId;
-                            if (e < total) {
-                                const uint32_t j = e / K, rk = e - j * K;
-                                const uint64_t wj = w0 + j;
-                                const uint32_t first_row = (uint32_t)(sk_start(wj, Q, G) / p.nq);
-                                const uint32_t* lw = reinterpret_cast<const uint32_t*>(
-                                    p.partials + (size_t)(2 * wj + (o == first_row ? 0 : 1)) * p.stride);
-                                x = __uint_as_float(__ldcg(lw + 4 + rk));
-                                id = __ldcg(lw + 4 + K + rk);
-                            }
-                            sel.L.insert32(x, id, lane);
-                        }
-                    }
+                    const bool tail0 = sk_start(w0, Q, G) != gr;
+                    merge_pieces<SLOTS, TOPK>(p, w0, pieces, tail0, lane, sel.L, C, S, has_xt, xt_row);
                     if (lane == 0) p.counters[w0] = 0u;  // ready for the next call
                 }
             }

@@ -18,10 +18,15 @@ constexpr uint32_t kMaxCtasPerSm = 4;           // launch cap; sizes the workspa
 constexpr uint32_t kMinPieceVec = 1024;         // 16 KB of logits per warp at least
 constexpr uint32_t kStageOffsetsMax = 2048;     // stage off/out_off in smem when B+1 <= this
 constexpr uint32_t kUnroll = LP_UNROLL;
+constexpr uint32_t kStages = LP_STAGES;
+constexpr size_t kRingBytes = lpk::ring_bytes<kUnroll, kStages>();
+// Largest dynamic shared memory a launch asks for: the rings + staged offsets/echo.
+constexpr size_t kMaxDynSmem = kRingBytes + 2 * kStageOffsetsMax * 4 + kStageOffsetsMax;
 constexpr int kVariants = 3;                    // levels 0 | 1..5 | 6
 
 struct DeviceInfo {
     bool ready = false;
+    bool smem_attr[kVariants] = {false, false, false};
     int sms = 0;
     int occ[kVariants] = {0, 0, 0};
     size_t occ_smem[kVariants] = {0, 0, 0};
@@ -32,9 +37,9 @@ DeviceInfo g_dev[kMaxDevices];
 
 const void* variant_fn(int v) {
     switch (v) {
-        case 0: return reinterpret_cast<const void*>(&lpk::k_rows<1, false, kUnroll>);
-        case 1: return reinterpret_cast<const void*>(&lpk::k_rows<1, true, kUnroll>);
-        default: return reinterpret_cast<const void*>(&lpk::k_rows<2, true, kUnroll>);
+        case 0: return reinterpret_cast<const void*>(&lpk::k_rows<1, false, kUnroll, kStages>);
+        case 1: return reinterpret_cast<const void*>(&lpk::k_rows<1, true, kUnroll, kStages>);
+        default: return reinterpret_cast<const void*>(&lpk::k_rows<2, true, kUnroll, kStages>);
     }
 }
 
@@ -59,6 +64,14 @@ bool device_info(int* dev_out, DeviceInfo** info) {
 
 int occupancy(DeviceInfo* d, int v, size_t smem) {
     std::lock_guard<std::mutex> lock(g_mu);
+    if (!d->smem_attr[v]) {
+        if (cudaFuncSetAttribute(variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        d->smem_attr[v] = true;
+    }
     if (d->occ[v] == 0 || d->occ_smem[v] != smem) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, variant_fn(v), lpk::kThreads, smem) != cudaSuccess)
@@ -71,6 +84,7 @@ int occupancy(DeviceInfo* d, int v, size_t smem) {
     return d->occ[v];
 }
 
+// Arrival counters: one u32 word per warp, padded to 256 B.
 size_t counters_bytes(uint32_t g_max) { return ((size_t)g_max * 4 + 255) & ~(size_t)255; }
 
 // Largest number of warps a launch can have on a device with `sms` SMs.
@@ -167,16 +181,18 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
     p.stride = lpk::partial_stride_bytes(K);
     p.min_piece = kMinPieceVec;
     p.stage_offsets = (B + 1u <= kStageOffsetsMax) ? 1u : 0u;
-    const size_t smem = p.stage_offsets ? (size_t)2 * (B + 1u) * sizeof(uint32_t) + ((B + 3u) & ~3u) : 0;
+
+    const size_t smem = kRingBytes + (p.stage_offsets ? (size_t)2 * (B + 1u) * sizeof(uint32_t) + ((B + 3u) & ~3u) : 0);
 
     const int v = variant_of(levels);
     const int occ = occupancy(d, v, smem);
+    if (occ == 0) return LP_ERR_CUDA;
     const uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;  // occ <= kMaxCtasPerSm
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (v) {
-        case 0: lpk::k_rows<1, false, kUnroll><<<grid, lpk::kThreads, smem, s>>>(p); break;
-        case 1: lpk::k_rows<1, true, kUnroll><<<grid, lpk::kThreads, smem, s>>>(p); break;
-        default: lpk::k_rows<2, true, kUnroll><<<grid, lpk::kThreads, smem, s>>>(p); break;
+        case 0: lpk::k_rows<1, false, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
+        case 1: lpk::k_rows<1, true, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
+        default: lpk::k_rows<2, true, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
     }
     if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
     return LP_OK;
@@ -210,7 +226,7 @@ const char* lp_ragged_strerror(lp_status status) {
 // ---------------------------------------------------------------------------------
 // Allocation-free variant of lp_ragged_compute.
 //
-// Its scratch (status word, per-CTA arrival counters, split-row partial tuples)
+// Its scratch (status word, arrival counters, split-row partial tuples)
 // lives in one file-scope device array instead of a caller-provided workspace.
 // Every GPU that loads this library holds the array until the process exits; all
 // calls on a device share it, so calls that overlap on the GPU (two streams, two
