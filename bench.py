@@ -47,7 +47,12 @@ WORKLOAD_TEXT = {
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the row kernel,
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "decode": {"bytes_per_launch": 136600576, "source_hash": "3c2d9fb646397a96",
+               "capture": "profiles/k_rows_decode.md"},
+    "prefill": {"bytes_per_launch": 904551680, "source_hash": "3c2d9fb646397a96",
+                "capture": "profiles/k_rows_prefill.md"},
+}
 
 
 def kernel_source_hash() -> str:
@@ -133,6 +138,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "window": window}
 
 
+# ------------------------------------------------------------------------ multi-rank
+def combine_over_ranks(values, dist, device="cpu"):
+    """Max of each timing over all ranks (each rank times its own batch; the job is as
+    slow as its slowest rank). With no process group, the values come back unchanged."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rows_per_s(rows_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Rows of all ranks divided by the (max-over-ranks) step time."""
+    return rows_per_rank * world / (ms_per_step / 1e3)
+
+
 # ------------------------------------------------------------------------ oracle leg
 def _oracle_row(args):
     import oracle
@@ -148,14 +170,22 @@ def cpu_cores() -> int:
 
 
 def oracle_sample(batch, n_rows: int, seed: int = 0):
-    """Copy n scored rows device->host with their targets (work items for the oracle)."""
+    """n scored rows (drawn with replacement once the workload's rows run out), copied
+    device->host with their targets: the work items for the oracle."""
     import numpy as np
     import oracle
     off, tokens, sampled, echo = batch.host()
     mapping = oracle.output_rows(off, echo, tokens, sampled)
     rng = np.random.default_rng(seed)
-    picks = rng.choice(len(mapping), size=min(n_rows, len(mapping)), replace=False)
-    return [(batch.logits[mapping[o][1]].cpu().numpy(), mapping[o][2], batch.levels) for o in picks]
+    picks = rng.choice(len(mapping), size=n_rows, replace=n_rows > len(mapping))
+    cache = {}
+    items = []
+    for o in picks:
+        r = mapping[o][1]
+        if r not in cache:
+            cache[r] = batch.logits[r].cpu().numpy()
+        items.append((cache[r], mapping[o][2], batch.levels))
+    return items
 
 
 def time_oracle(batch, target_cpu_s: float, pool, cores: int, items=None):
@@ -264,10 +294,7 @@ def run_ours(args, rank: int, world: int, dist):
     ms_total = t_start.elapsed_time(t_end)
     ms_step = ms_total / args.steps
     compute_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
-    if dist is not None:
-        t = torch.tensor([ms_step, compute_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, compute_ms = float(t[0]), float(t[1])
+    ms_step, compute_ms = combine_over_ranks([ms_step, compute_ms], dist, dev)
     clocks = sampler.summary(w0, w1)
     status = lp.read_status(ws)
     if status != 0:
@@ -310,11 +337,8 @@ def run_ours(args, rank: int, world: int, dist):
         eb.record(stream)
         torch.cuda.synchronize()
         e2e_ms = ea.elapsed_time(eb) / k_e2e
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t[0])
-        e2e = {"value": R * world / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+        e2e_ms = combine_over_ranks([e2e_ms], dist, dev)[0]
+        e2e = {"value": whole_job_rows_per_s(R, world, e2e_ms), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": k_e2e}
 
     alg = algorithmic_bytes(R, V, W, B)
@@ -337,11 +361,11 @@ def run_ours(args, rank: int, world: int, dist):
         with mp.get_context("spawn").Pool(cores) as pool:
             n, dt = time_oracle(batch, args.cpu_seconds, pool, cores)
         cpu = {"value": n / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n} random scored rows of this workload (numpy fp64 oracle, full sort per row), "
-                         f"{dt:.1f} s wall over a spawn pool of {cores} processes"}
+               "sample": f"{n} scored rows of this workload drawn at random (numpy fp64 oracle, full sort "
+                         f"per row), {dt:.1f} s wall over a spawn pool of {cores} processes"}
 
     line = {
-        "metric": METRIC, "value": R * world / (ms_step / 1e3), "unit": "rows/s", "n_gpus": world,
+        "metric": METRIC, "value": whole_job_rows_per_s(R, world, ms_step), "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "B": B, "T": T, "V": V,

@@ -47,15 +47,6 @@ __device__ __forceinline__ bool better(float xa, uint32_t ia, float xb, uint32_t
     return xa > xb || (xa == xb && ia < ib);
 }
 
-// Order-preserving map float -> uint32 (for atomicMax on a shared threshold).
-__device__ __forceinline__ uint32_t f2ord(float f) {
-    uint32_t b = __float_as_uint(f);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float ord2f(uint32_t o) {
-    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
-}
-
 __device__ __forceinline__ float pick(const float4& v, int k) {
     return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
@@ -174,24 +165,6 @@ __device__ __forceinline__ void warp_lse2_reduce(float& c, float& s) {
         float oc = __shfl_xor_sync(kFull, c, o);
         float os = __shfl_xor_sync(kFull, s, o);
         lse2_combine(c, s, oc, os);
-    }
-}
-
-// Combine two (max, sum of exp(x - max)) pairs.
-__device__ __forceinline__ void lse_combine(float& m, float& s, float om, float os) {
-    float M = fmaxf(m, om);
-    float a = (m == neg_inf()) ? 0.f : s * ex2((m - M) * kLog2e);
-    float b = (om == neg_inf()) ? 0.f : os * ex2((om - M) * kLog2e);
-    m = M;
-    s = a + b;
-}
-
-__device__ __forceinline__ void warp_lse_reduce(float& m, float& s) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        float om = __shfl_xor_sync(kFull, m, o);
-        float os = __shfl_xor_sync(kFull, s, o);
-        lse_combine(m, s, om, os);
     }
 }
 
