@@ -132,7 +132,7 @@ lp_status lp_ragged_compute(const float *logits, uint32_t T, uint32_t V,
  *   capture. Each call zeroes the status word and arrival counters first, and no
  *   allocating routine (cudaMalloc, cudaFree, a library allocator) is called.
  *   Returns LP_ERR_WORKSPACE when this GPU needs more scratch than the array holds
- *   (more than ~230 SMs at levels 6). All calls share the array: calls that overlap
+ *   (more than ~245 SMs at levels 6). All calls share the array: calls that overlap
  *   on the GPU (other streams, other host threads) race; serialise them.
  */
 #define LP_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
