@@ -85,6 +85,21 @@ __device__ __forceinline__ void bitonic_sort32(float& x, uint32_t& id, int lane)
     }
 }
 
+// K-th largest (K <= 32) of one float per lane, broadcast to the warp: bitonic sort of
+// the 32 values, descending, then lane K-1.
+__device__ __forceinline__ float kth_largest32(float v, uint32_t K, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const float o = __shfl_xor_sync(kFull, v, j);
+            const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+            v = keep_max ? fmaxf(v, o) : fminf(v, o);
+        }
+    }
+    return __shfl_sync(kFull, v, (K - 1) & 31);
+}
+
 // a := best 32*SLOTS of (a U b); both sorted descending in the lane-major layout.
 template <int SLOTS>
 __device__ __forceinline__ void merge_lists(float (&ax)[SLOTS], uint32_t (&ai)[SLOTS],

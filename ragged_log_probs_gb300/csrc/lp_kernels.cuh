@@ -44,6 +44,7 @@ namespace lpk {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr uint32_t kThrEvery = 4;  // blocks between lane-maximum threshold refreshes (power of 2)
 constexpr int kPlanThreads = 1024;
 constexpr uint32_t kStatusOffsets = 1u << 4;     // bit of LP_ERR_OFFSETS
 constexpr uint32_t kStatusTokenRange = 1u << 5;  // bit of LP_ERR_TOKEN_RANGE
@@ -330,7 +331,18 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
         for (int u = 1; u < U; ++u) acc = fadd2(acc, ls.term4(v[u]));
         ls.s += acc.x + acc.y;
 
-        if constexpr (TOPK) {
+        if constexpr (TOPK && SLOTS == 1) {
+            // The K-th largest of the 32 lanes' running maxima is the value of K distinct
+            // elements already seen, so no element below it can be in the top-k: a
+            // threshold that follows the warp's true K-th best at the cost of one float
+            // sort, refreshed on the first block and then every kThrEvery blocks.
+            if ((blk & (kThrEvery - 1)) == 0) sel.thr = fmaxf(sel.thr, kth_largest32(ls.m, sel.K, lane));
+            if (__any_sync(kFull, bm >= sel.thr)) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr), lane);
+            }
+        }
+        if constexpr (TOPK && SLOTS == 2) {
             if (blk == 0 && sel.cnt == 0 && sel.thr == neg_inf()) {
                 // Seed the list with each lane's best (and second best) element of this
                 // block, scanned in id order, so the threshold is useful at once.
