@@ -38,7 +38,13 @@ namespace lpk {
 #define LP_MIN_BLOCKS 3
 #endif
 #ifndef LP_STAGES
-#define LP_STAGES 4  // blocks per warp in the shared-memory ring (power of two)
+#define LP_STAGES 4  // blocks per warp in the shared-memory ring
+#endif
+#ifndef LP_QUEUE_WARPS
+#define LP_QUEUE_WARPS 8  // warps per CTA of the row-queue kernel
+#endif
+#ifndef LP_QUEUE_STAGES
+#define LP_QUEUE_STAGES 4  // ring depth of the row-queue kernel
 #endif
 
 
@@ -82,6 +88,7 @@ struct RowsParams {
     uint32_t stride;         // partial slot bytes
     uint32_t min_piece;      // minimum vectors per warp
     uint32_t stage_offsets;  // 1: copy off / out_off / echo to shared memory
+    uint32_t num_sms;        // SMs of the device (row-queue kernel: rows per SM cap)
 };
 
 // ---------------------------------------------------------------------------------
@@ -296,7 +303,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     auto issue = [&](uint32_t blk) {
         if (blk < nblk) {
             const float* src = vp + (size_t)blk * 128u * U;
-            const uint32_t dst = ring_lane + (blk & (STAGES - 1)) * (U * 512u);
+            const uint32_t dst = ring_lane + (blk % STAGES) * (U * 512u);
 #pragma unroll
             for (int u = 0; u < U; ++u) cp_async16(dst + 512u * u, src + 128 * u);
         }
@@ -311,7 +318,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
         issue(blk + STAGES - 1);
         cp_async_wait<STAGES - 1>();
         float4 v[U];
-        const float4* stage = ring + (blk & (STAGES - 1)) * (U * 32u) + lane;
+        const float4* stage = ring + (blk % STAGES) * (U * 32u) + lane;
 #pragma unroll
         for (int u = 0; u < U; ++u) v[u] = stage[32 * u];
         if (xt_pending) {  // the target id has arrived by now
@@ -648,6 +655,174 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
         q0 = 0;
         ++o;
         while (b + 1 < B && out_off[b + 1] <= o) ++b;
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// Few rows (each row much larger than a warp's share, e.g. next-token logits for a
+// decode batch): CTAs of NW warps take whole rows from a queue (one atomic counter)
+// and split each row into NW contiguous parts, one per warp; the warps' results are
+// merged in shared memory, so no row goes through global partials or tickets. At most
+// ceil(R / SMs) CTAs of an SM take part (a per-SM slot counter), so all rows stream at
+// once and no SM carries more than its share. The last CTA to leave resets the queue
+// words and the per-SM counters for the next call.
+template <int NW>
+struct CtaMerge {
+    float list_x[NW][64];
+    uint32_t list_i[NW][64];
+    float red_c[NW];
+    float red_s[NW];
+    float xt;
+    uint32_t has_xt;
+    uint32_t row;
+};
+
+constexpr int kQueueWarps = LP_QUEUE_WARPS;
+constexpr int kQueueStages = LP_QUEUE_STAGES;
+
+template <int SLOTS, bool TOPK, int U, int STAGES, int NW>
+__global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    float4* rings = reinterpret_cast<float4*>(s_raw);
+    uint32_t* s_dyn = reinterpret_cast<uint32_t*>(s_raw + (size_t)NW * STAGES * U * 512u);
+    __shared__ float s_cx[NW][64];
+    __shared__ uint32_t s_ci[NW][64];
+    __shared__ CtaMerge<NW> cm;
+    constexpr int kT = NW * 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t B = p.B, V = p.V, K = p.K;
+
+    const uint32_t status = __ldcg(p.status);
+    const uint32_t R = __ldcg(p.out_off + B);
+    const uint32_t* off = p.off;
+    const uint32_t* out_off = p.out_off;
+    const uint8_t* echo = p.echo;
+    if (p.stage_offsets) {
+        for (uint32_t i = threadIdx.x; i <= B; i += kT) {
+            const uint32_t a0 = p.off[i], a1 = p.out_off[i];
+            const uint8_t e = i < B ? p.echo[i] : 0;
+            s_dyn[i] = a0;
+            s_dyn[B + 1 + i] = a1;
+            if (i < B) reinterpret_cast<uint8_t*>(s_dyn + 2 * (B + 1))[i] = e;
+        }
+        off = s_dyn;
+        out_off = s_dyn + B + 1;
+        echo = reinterpret_cast<const uint8_t*>(s_dyn + 2 * (B + 1));
+    }
+    if (threadIdx.x == 0) cm.has_xt = 0u;
+    uint32_t* queue = p.counters;  // [0] next row, [1] CTAs finished, [2 + sm] CTAs of that SM
+    bool bad = (status & kStatusOffsets) || R > p.T;
+    if (threadIdx.x == 0) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        const uint32_t slot = atomicAdd(queue + 2 + smid % p.num_sms, 1u);
+        const uint32_t cap = p.num_sms ? (R + p.num_sms - 1) / p.num_sms : 1u;
+        cm.row = slot < cap ? 1u : 0u;  // this CTA takes part
+    }
+    __syncthreads();
+    const bool takes_part = cm.row != 0;
+    __syncthreads();
+    if (threadIdx.x == 0 && blockIdx.x == 0 && R > p.T && !(status & kStatusOffsets))
+        atomicOr(p.status, kStatusOffsets);
+    float4* ring = rings + (size_t)w * STAGES * U * 32;
+
+    for (;;) {
+        if (threadIdx.x == 0) cm.row = (bad || !takes_part) ? R : atomicAdd(queue, 1u);
+        __syncthreads();
+        const uint32_t o = cm.row;
+        if (o >= R) break;
+        uint32_t lo = 0, hi = B;  // batch of row o
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (out_off[mid] <= o) lo = mid; else hi = mid;
+        }
+        const uint32_t b = lo;
+        const uint32_t ob = out_off[b], oe = out_off[b + 1];
+        const uint32_t sb = off[b], eb = off[b + 1];
+        const uint32_t cnt = oe - ob, len = eb - sb;
+        const bool valid = (o >= ob) && (o < oe) && (eb > sb) && (eb <= p.T) &&
+                           (cnt == (echo[b] ? len : 1u));
+        if (!valid) {
+            if (w == 0) {
+                for (uint32_t col = (uint32_t)lane; col < p.W; col += 32) {
+                    p.out_lp[(size_t)o * p.W + col] = __int_as_float(0x7fc00000);
+                    p.out_tok[(size_t)o * p.W + col] = kPadId;
+                }
+                if (lane == 0) atomicOr(p.status, kStatusOffsets);
+            }
+            __syncthreads();
+            continue;
+        }
+        const uint32_t r = eb - cnt + (o - ob);
+        const uint32_t t = (r + 1 < eb) ? p.tokens[r + 1] : p.sampled[b];
+        const float* rowp = p.logits + (size_t)r * V;
+        const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
+        const uint32_t wq0 = (uint32_t)(((uint64_t)p.nq * w) / NW);
+        const uint32_t wq1 = (uint32_t)(((uint64_t)p.nq * (w + 1)) / NW);
+        const int64_t e_lo = 4 * (int64_t)wq0 - a, e_hi = 4 * (int64_t)wq1 - a;
+        const bool t_here = t < V && (int64_t)t >= e_lo && (int64_t)t < e_hi;
+
+        LaneSum ls;
+        ls.init();
+        Selector<SLOTS> sel;
+        sel.init(s_cx[w], s_ci[w], K);
+        float xt = 0.f;
+        stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t, xt, ring);
+
+        float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, S = ls.s;
+        warp_lse2_reduce(C, S);
+        if (lane == 0) {
+            cm.red_c[w] = C;
+            cm.red_s[w] = S;
+            if (t_here) { cm.xt = xt; cm.has_xt = 1u; }
+        }
+        if constexpr (TOPK) {
+#pragma unroll
+            for (int k = 0; k < SLOTS; ++k) {
+                cm.list_x[w][lane + 32 * k] = sel.L.x[k];
+                cm.list_i[w][lane + 32 * k] = sel.L.id[k];
+            }
+        }
+        __syncthreads();
+        if constexpr (TOPK) {
+#pragma unroll
+            for (int st = 1; st < NW; st <<= 1) {
+                if ((w & (2 * st - 1)) == 0 && w + st < NW) {
+                    float bx[SLOTS];
+                    uint32_t bi[SLOTS];
+#pragma unroll
+                    for (int k = 0; k < SLOTS; ++k) {
+                        bx[k] = cm.list_x[w + st][lane + 32 * k];
+                        bi[k] = cm.list_i[w + st][lane + 32 * k];
+                    }
+                    merge_lists<SLOTS>(sel.L.x, sel.L.id, bx, bi, lane);
+#pragma unroll
+                    for (int k = 0; k < SLOTS; ++k) {
+                        cm.list_x[w][lane + 32 * k] = sel.L.x[k];
+                        cm.list_i[w][lane + 32 * k] = sel.L.id[k];
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        if (w == 0) {
+            C = neg_inf();
+            S = 0.f;
+            for (int j = lane; j < NW; j += 32) lse2_combine(C, S, cm.red_c[j], cm.red_s[j]);
+            warp_lse2_reduce(C, S);
+            write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, lane);
+            __syncwarp();
+            if (lane == 0) cm.has_xt = 0u;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {  // last CTA out: ready for the next call
+            queue[0] = 0u;
+            queue[1] = 0u;
+            for (uint32_t i = 0; i < p.num_sms; ++i) queue[2 + i] = 0u;
+        }
     }
 }
 

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "lp_kernels.cuh"
@@ -22,14 +24,21 @@ constexpr uint32_t kStages = LP_STAGES;
 constexpr size_t kRingBytes = lpk::ring_bytes<kUnroll, kStages>();
 // Largest dynamic shared memory a launch asks for: the rings + staged offsets/echo.
 constexpr size_t kMaxDynSmem = kRingBytes + 2 * kStageOffsetsMax * 4 + kStageOffsetsMax;
-constexpr int kVariants = 3;                    // levels 0 | 1..5 | 6
+constexpr int kQW = lpk::kQueueWarps;  // warps per CTA of the row-queue kernel
+constexpr int kQS = lpk::kQueueStages;
+constexpr size_t kQueueRingBytes = (size_t)kQW * kQS * kUnroll * 512;
+constexpr size_t kMaxDynSmemQueue = kQueueRingBytes + 2 * kStageOffsetsMax * 4 + kStageOffsetsMax;
+// Dynamic shared memory the row-queue kernel may ask for next to its ~17 KB of static
+// shared memory (227 KB per CTA in all).
+constexpr size_t kQueueDynSmemBudget = 208 * 1024;
+constexpr int kVariants = 6;                    // (levels 0 | 1..5 | 6) x (warp ranges | row queue)
 
 struct DeviceInfo {
     bool ready = false;
-    bool smem_attr[kVariants] = {false, false, false};
+    bool smem_attr[kVariants] = {};
     int sms = 0;
-    int occ[kVariants] = {0, 0, 0};
-    size_t occ_smem[kVariants] = {0, 0, 0};
+    int occ[kVariants] = {};
+    size_t occ_smem[kVariants] = {};
 };
 
 std::mutex g_mu;
@@ -39,7 +48,10 @@ const void* variant_fn(int v) {
     switch (v) {
         case 0: return reinterpret_cast<const void*>(&lpk::k_rows<1, false, kUnroll, kStages>);
         case 1: return reinterpret_cast<const void*>(&lpk::k_rows<1, true, kUnroll, kStages>);
-        default: return reinterpret_cast<const void*>(&lpk::k_rows<2, true, kUnroll, kStages>);
+        case 2: return reinterpret_cast<const void*>(&lpk::k_rows<2, true, kUnroll, kStages>);
+        case 3: return reinterpret_cast<const void*>(&lpk::k_rows_cta<1, false, kUnroll, kQS, kQW>);
+        case 4: return reinterpret_cast<const void*>(&lpk::k_rows_cta<1, true, kUnroll, kQS, kQW>);
+        default: return reinterpret_cast<const void*>(&lpk::k_rows_cta<2, true, kUnroll, kQS, kQW>);
     }
 }
 
@@ -65,8 +77,8 @@ bool device_info(int* dev_out, DeviceInfo** info) {
 int occupancy(DeviceInfo* d, int v, size_t smem) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!d->smem_attr[v]) {
-        if (cudaFuncSetAttribute(variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem) !=
-            cudaSuccess) {
+        if (cudaFuncSetAttribute(variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(v >= 3 ? kMaxDynSmemQueue : kMaxDynSmem)) != cudaSuccess) {
             (void)cudaGetLastError();
             return 0;
         }
@@ -74,7 +86,8 @@ int occupancy(DeviceInfo* d, int v, size_t smem) {
     }
     if (d->occ[v] == 0 || d->occ_smem[v] != smem) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, variant_fn(v), lpk::kThreads, smem) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, variant_fn(v), v >= 3 ? kQW * 32 : lpk::kThreads,
+                                                          smem) != cudaSuccess)
             n = 1;
         if (n < 1) n = 1;
         if (n > (int)kMaxCtasPerSm) n = kMaxCtasPerSm;
@@ -181,18 +194,41 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
     p.stride = lpk::partial_stride_bytes(K);
     p.min_piece = kMinPieceVec;
     p.stage_offsets = (B + 1u <= kStageOffsetsMax) ? 1u : 0u;
+    p.num_sms = (uint32_t)d->sms;
 
     const size_t smem = kRingBytes + (p.stage_offsets ? (size_t)2 * (B + 1u) * sizeof(uint32_t) + ((B + 3u) & ~3u) : 0);
 
-    const int v = variant_of(levels);
-    const int occ = occupancy(d, v, smem);
+    // Row queue when even all-echo input (R <= T) gives fewer rows than half the warps;
+    // otherwise warp-owned ranges of the row space (the two kernels give the same result).
+    int v = variant_of(levels);
+    int occ = occupancy(d, v, smem);
     if (occ == 0) return LP_ERR_CUDA;
-    const uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;  // occ <= kMaxCtasPerSm
+    uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;  // occ <= kMaxCtasPerSm
+    const char* force = std::getenv("LP_RAGGED_KERNEL");  // test hook: "warp" or "queue"
+    bool queue = 2ull * T < (uint64_t)grid * lpk::kWarps;
+    if (force && std::strcmp(force, "warp") == 0) queue = false;
+    if (force && std::strcmp(force, "queue") == 0) queue = true;
+    size_t launch_smem = smem;
+    if (queue) {
+        v += 3;
+        launch_smem = smem - kRingBytes + kQueueRingBytes;
+        if (launch_smem > kQueueDynSmemBudget) {  // very many batches: read offsets from global memory
+            p.stage_offsets = 0;
+            launch_smem = kQueueRingBytes;
+        }
+        occ = occupancy(d, v, launch_smem);
+        if (occ == 0) return LP_ERR_CUDA;
+        grid = (uint32_t)d->sms * (uint32_t)occ;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint32_t qthreads = kQW * 32;
     switch (v) {
         case 0: lpk::k_rows<1, false, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
         case 1: lpk::k_rows<1, true, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
-        default: lpk::k_rows<2, true, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
+        case 2: lpk::k_rows<2, true, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
+        case 3: lpk::k_rows_cta<1, false, kUnroll, kQS, kQW><<<grid, qthreads, launch_smem, s>>>(p); break;
+        case 4: lpk::k_rows_cta<1, true, kUnroll, kQS, kQW><<<grid, qthreads, launch_smem, s>>>(p); break;
+        default: lpk::k_rows_cta<2, true, kUnroll, kQS, kQW><<<grid, qthreads, launch_smem, s>>>(p); break;
     }
     if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
     return LP_OK;

@@ -153,3 +153,28 @@ def test_bad_offsets_detected_on_device():
     with pytest.raises(lp.LpError):
         lp.ragged_log_probs(x, off, torch.zeros(6, dtype=torch.int32, device="cuda"),
                             torch.zeros(3, dtype=torch.int32, device="cuda"), echo, 3)
+
+
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
+@pytest.mark.parametrize("name,kw", [("decode", dict(B=40)), ("prefill", dict(B=3, max_len=90)),
+                                     ("mixed", dict(B=9, max_len=20)), ("wide", dict(B=2, max_len=12)),
+                                     ("tiny", dict())])
+def test_both_kernels(kernel, name, kw, monkeypatch):
+    # Warp-owned ranges and the CTA row queue must give the same result on every shape.
+    monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
+    parity.check_batch(workloads.make_batch(name, "cuda", **kw), what=f"{name}/{kernel}")
+
+
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
+def test_both_kernels_edge_rows(kernel, monkeypatch):
+    monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(7, 4097, generator=g)
+    x[2, :] = float("-inf")
+    x[4, 7:] = float("-inf")
+    parity.check_batch(_custom(x, [2, 5], [1, 1], 6), what=f"edge/{kernel}")
+    b = workloads.make_next_token_batch(3, 200003, levels=3, device="cuda", seed=12)
+    ws = lp.new_workspace(b.B, b.T, b.V, b.levels)
+    first = parity.run_gpu(b, workspace=ws)
+    again = parity.run_gpu(b, workspace=ws)      # queue words and tickets were reset
+    assert np.array_equal(first[2], again[2]) and np.array_equal(first[1], again[1], equal_nan=True)
