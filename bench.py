@@ -48,9 +48,9 @@ WORKLOAD_TEXT = {
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 136600576, "source_hash": "3c2d9fb646397a96",
-               "capture": "profiles/k_rows_decode.md"},
-    "prefill": {"bytes_per_launch": 904551680, "source_hash": "3c2d9fb646397a96",
+    "decode": {"bytes_per_launch": 135671040, "source_hash": "20203a29c7034b56",
+               "capture": "profiles/k_rows_cta_decode.md"},
+    "prefill": {"bytes_per_launch": 904610560, "source_hash": "20203a29c7034b56",
                 "capture": "profiles/k_rows_prefill.md"},
 }
 
@@ -61,6 +61,13 @@ def kernel_source_hash() -> str:
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def rows_kernel_warps() -> int:
+    """Warps of the warp-range kernel's grid (152 SMs x 3 CTAs x 8 warps on GB300);
+    the library picks the row-queue kernel when 2*T is below this."""
+    import torch
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count * 3 * 8
 
 
 def algorithmic_bytes(R: int, V: int, W: int, B: int) -> int:
@@ -348,7 +355,9 @@ def run_ours(args, rank: int, world: int, dist):
     rec = NCU_TRAFFIC.get(args.config)
     if rec and rec.get("source_hash") == kernel_source_hash():
         traffic = rec["bytes_per_launch"]
-    roofline = {"bound": "hbm", "kernel": "k_rows (lp_ragged_compute)", "achieved": round(achieved, 1),
+    kernel_name = ("k_rows_cta (lp_ragged_compute, row queue)" if 2 * T < rows_kernel_warps()
+                   else "k_rows (lp_ragged_compute, warp ranges)")
+    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
