@@ -43,6 +43,12 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Programmatic dependent launch: the producer lets the next kernel on the stream start
+// launching; the consumer waits here until the producer has finished and its writes
+// are visible (a no-op when the kernel was launched without the dependency).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ bool better(float xa, uint32_t ia, float xb, uint32_t ib) {
     return xa > xb || (xa == xb && ia < ib);
 }

@@ -46,6 +46,9 @@ namespace lpk {
 #ifndef LP_QUEUE_STAGES
 #define LP_QUEUE_STAGES 4  // ring depth of the row-queue kernel
 #endif
+#ifndef LP_QUEUE_UNROLL
+#define LP_QUEUE_UNROLL 4  // vectors per lane per block in the row-queue kernel
+#endif
 
 
 constexpr int kWarps = 8;
@@ -101,6 +104,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(const uint32_t* __restric
     __shared__ uint32_t s_warp[kPlanThreads / 32];
     __shared__ uint32_t s_carry;
     __shared__ uint32_t s_bad;
+    pdl_launch_dependents();  // the row kernel may launch now; it waits for our writes
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     if (tid == 0) { s_carry = 0; s_bad = 0; }
     for (uint32_t i = tid; i < n_counters; i += kPlanThreads) counters[i] = 0;
@@ -547,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t B = p.B, V = p.V, K = p.K;
 
+    pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
     // Status, row count and the offsets are fetched in one round trip.
     const uint32_t status = __ldcg(p.status);
     const uint32_t R = __ldcg(p.out_off + B);
@@ -679,6 +684,7 @@ struct CtaMerge {
 
 constexpr int kQueueWarps = LP_QUEUE_WARPS;
 constexpr int kQueueStages = LP_QUEUE_STAGES;
+constexpr int kQueueUnroll = LP_QUEUE_UNROLL;
 
 template <int SLOTS, bool TOPK, int U, int STAGES, int NW>
 __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
@@ -692,6 +698,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t B = p.B, V = p.V, K = p.K;
 
+    pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
     const uint32_t status = __ldcg(p.status);
     const uint32_t R = __ldcg(p.out_off + B);
     const uint32_t* off = p.off;

@@ -26,11 +26,15 @@ constexpr size_t kRingBytes = lpk::ring_bytes<kUnroll, kStages>();
 constexpr size_t kMaxDynSmem = kRingBytes + 2 * kStageOffsetsMax * 4 + kStageOffsetsMax;
 constexpr int kQW = lpk::kQueueWarps;  // warps per CTA of the row-queue kernel
 constexpr int kQS = lpk::kQueueStages;
-constexpr size_t kQueueRingBytes = (size_t)kQW * kQS * kUnroll * 512;
+constexpr int kQU = lpk::kQueueUnroll;
+constexpr size_t kQueueRingBytes = (size_t)kQW * kQS * kQU * 512;
 constexpr size_t kMaxDynSmemQueue = kQueueRingBytes + 2 * kStageOffsetsMax * 4 + kStageOffsetsMax;
 // Dynamic shared memory the row-queue kernel may ask for next to its ~17 KB of static
 // shared memory (227 KB per CTA in all).
 constexpr size_t kQueueDynSmemBudget = 208 * 1024;
+#ifndef LP_PDL
+#define LP_PDL 1  // launch the row kernel as a programmatic dependent of the plan
+#endif
 constexpr int kVariants = 6;                    // (levels 0 | 1..5 | 6) x (warp ranges | row queue)
 
 struct DeviceInfo {
@@ -49,9 +53,9 @@ const void* variant_fn(int v) {
         case 0: return reinterpret_cast<const void*>(&lpk::k_rows<1, false, kUnroll, kStages>);
         case 1: return reinterpret_cast<const void*>(&lpk::k_rows<1, true, kUnroll, kStages>);
         case 2: return reinterpret_cast<const void*>(&lpk::k_rows<2, true, kUnroll, kStages>);
-        case 3: return reinterpret_cast<const void*>(&lpk::k_rows_cta<1, false, kUnroll, kQS, kQW>);
-        case 4: return reinterpret_cast<const void*>(&lpk::k_rows_cta<1, true, kUnroll, kQS, kQW>);
-        default: return reinterpret_cast<const void*>(&lpk::k_rows_cta<2, true, kUnroll, kQS, kQW>);
+        case 3: return reinterpret_cast<const void*>(&lpk::k_rows_cta<1, false, kQU, kQS, kQW>);
+        case 4: return reinterpret_cast<const void*>(&lpk::k_rows_cta<1, true, kQU, kQS, kQW>);
+        default: return reinterpret_cast<const void*>(&lpk::k_rows_cta<2, true, kQU, kQS, kQW>);
     }
 }
 
@@ -220,16 +224,28 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
         if (occ == 0) return LP_ERR_CUDA;
         grid = (uint32_t)d->sms * (uint32_t)occ;
     }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const uint32_t qthreads = kQW * 32;
+    // Launched as a programmatic dependent of the previous kernel on the stream (normally
+    // lp_ragged_plan): its CTAs become resident while the plan runs and wait on device.
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(v >= 3 ? kQW * 32 : lpk::kThreads);
+    cfg.dynamicSmemBytes = launch_smem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = LP_PDL ? 1 : 0;
+    cudaError_t err;
     switch (v) {
-        case 0: lpk::k_rows<1, false, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
-        case 1: lpk::k_rows<1, true, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
-        case 2: lpk::k_rows<2, true, kUnroll, kStages><<<grid, lpk::kThreads, smem, s>>>(p); break;
-        case 3: lpk::k_rows_cta<1, false, kUnroll, kQS, kQW><<<grid, qthreads, launch_smem, s>>>(p); break;
-        case 4: lpk::k_rows_cta<1, true, kUnroll, kQS, kQW><<<grid, qthreads, launch_smem, s>>>(p); break;
-        default: lpk::k_rows_cta<2, true, kUnroll, kQS, kQW><<<grid, qthreads, launch_smem, s>>>(p); break;
+        case 0: err = cudaLaunchKernelEx(&cfg, lpk::k_rows<1, false, kUnroll, kStages>, p); break;
+        case 1: err = cudaLaunchKernelEx(&cfg, lpk::k_rows<1, true, kUnroll, kStages>, p); break;
+        case 2: err = cudaLaunchKernelEx(&cfg, lpk::k_rows<2, true, kUnroll, kStages>, p); break;
+        case 3: err = cudaLaunchKernelEx(&cfg, lpk::k_rows_cta<1, false, kQU, kQS, kQW>, p); break;
+        case 4: err = cudaLaunchKernelEx(&cfg, lpk::k_rows_cta<1, true, kQU, kQS, kQW>, p); break;
+        default: err = cudaLaunchKernelEx(&cfg, lpk::k_rows_cta<2, true, kQU, kQS, kQW>, p); break;
     }
+    if (err != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
     if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
     return LP_OK;
 }
