@@ -53,6 +53,16 @@ __device__ __forceinline__ bool better(float xa, uint32_t ia, float xb, uint32_t
     return xa > xb || (xa == xb && ia < ib);
 }
 
+// Order-preserving map float -> uint32 (atomicMax on a shared threshold word; 0 decodes
+// to NaN, which fmaxf ignores, so a zeroed word means "no threshold yet").
+__device__ __forceinline__ uint32_t f2ord(float f) {
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord2f(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
 __device__ __forceinline__ float pick(const float4& v, int k) {
     return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }

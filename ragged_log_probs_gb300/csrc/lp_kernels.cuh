@@ -289,7 +289,7 @@ __device__ __forceinline__ float4 load_checked(const float* rowp, const float* v
 template <int SLOTS, bool TOPK, int U, int STAGES>
 __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint32_t q0, uint32_t q1, int lane,
                                              LaneSum& ls, Selector<SLOTS>& sel, bool t_here, uint32_t t,
-                                             float& xt, float4* ring) {
+                                             float& xt, float4* ring, uint32_t* shared_thr = nullptr) {
     const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
     const float* vbase = rowp - a;  // 16-byte aligned
     const uint32_t qf = a ? 1u : 0u;
@@ -347,7 +347,13 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
             // elements already seen, so no element below it can be in the top-k: a
             // threshold that follows the warp's true K-th best at the cost of one float
             // sort, refreshed on the first block and then every kThrEvery blocks.
-            if ((blk & (kThrEvery - 1)) == 0) sel.thr = fmaxf(sel.thr, kth_largest32(ls.m, sel.K, lane));
+            if ((blk & (kThrEvery - 1)) == 0) {
+                sel.thr = fmaxf(sel.thr, kth_largest32(ls.m, sel.K, lane));
+                if (shared_thr != nullptr) {  // warps on the same row share their thresholds
+                    if (lane == 0 && sel.thr != neg_inf()) atomicMax(shared_thr, f2ord(sel.thr));
+                    sel.thr = fmaxf(sel.thr, ord2f(*(volatile uint32_t*)shared_thr));
+                }
+            }
             if (__any_sync(kFull, bm >= sel.thr)) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr), lane);
@@ -680,6 +686,7 @@ struct CtaMerge {
     float xt;
     uint32_t has_xt;
     uint32_t row;
+    uint32_t thr;  // threshold shared by the warps of the CTA for the current row
 };
 
 constexpr int kQueueWarps = LP_QUEUE_WARPS;
@@ -716,7 +723,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         out_off = s_dyn + B + 1;
         echo = reinterpret_cast<const uint8_t*>(s_dyn + 2 * (B + 1));
     }
-    if (threadIdx.x == 0) cm.has_xt = 0u;
+    if (threadIdx.x == 0) { cm.has_xt = 0u; cm.thr = 0u; }
     uint32_t* queue = p.counters;  // [0] next row, [1] CTAs finished, [2 + sm] CTAs of that SM
     bool bad = (status & kStatusOffsets) || R > p.T;
     if (threadIdx.x == 0) {
@@ -774,7 +781,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         Selector<SLOTS> sel;
         sel.init(s_cx[w], s_ci[w], K);
         float xt = 0.f;
-        stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t, xt, ring);
+        stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t, xt, ring, &cm.thr);
 
         float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, S = ls.s;
         warp_lse2_reduce(C, S);
@@ -819,7 +826,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             warp_lse2_reduce(C, S);
             write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, lane);
             __syncwarp();
-            if (lane == 0) cm.has_xt = 0u;
+            if (lane == 0) { cm.has_xt = 0u; cm.thr = 0u; }
         }
         __syncthreads();
     }
