@@ -178,3 +178,33 @@ def test_both_kernels_edge_rows(kernel, monkeypatch):
     first = parity.run_gpu(b, workspace=ws)
     again = parity.run_gpu(b, workspace=ws)      # queue words and tickets were reset
     assert np.array_equal(first[2], again[2]) and np.array_equal(first[1], again[1], equal_nan=True)
+
+
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
+@pytest.mark.parametrize("levels", [1, 2, 3])
+def test_top_elements_in_one_lane(kernel, levels, monkeypatch):
+    # Rows whose top-k sits in few lanes' elements or is decided by ties: all-equal rows,
+    # coarse ties, top values planted in one lane's vectors, a row of few finite values.
+    monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
+    g = torch.Generator().manual_seed(20 + levels)
+    V = 40000
+    x = torch.randn(8, V, generator=g)
+    x[0, :] = 1.5
+    x[1] = torch.round(x[1] * 2) / 2
+    for j, pos in enumerate([0, 1, 2, 3, 128, 129, 130, 131]):
+        x[2, pos] = 10.0 - 0.25 * j
+    for j in range(8):
+        x[3, 4 * 7 + 512 * j] = 9.0 + j
+    x[4, :] = float("-inf")
+    x[4, 5:12] = 2.0
+    b = _custom(x, [3, 5], [1, 1], levels, seed=levels)
+    parity.check_batch(b, what=f"one-lane/{kernel}/levels{levels}")
+
+
+@pytest.mark.parametrize("V", [4093, 40001])
+def test_top_elements_in_one_lane_misaligned(V):
+    g = torch.Generator().manual_seed(V)
+    x = torch.randn(6, V, generator=g)
+    x[1, :] = 0.25
+    x[2, 1:9] = 50.0
+    parity.check_batch(_custom(x, [6], [1], 3, seed=V), what=f"one-lane-misaligned/{V}")
