@@ -6,6 +6,7 @@ CPU-baseline legs of ``bench.py``; never by the ``ragged_log_probs_gb300`` packa
 
 from .ragged_oracle import (  # noqa: F401
     PAD_ID,
+    assemble,
     levels_for_top_n,
     out_per_token,
     output_row_offsets,

@@ -209,3 +209,35 @@ def ragged_log_probs(logits: RowSource, logit_row_offsets: Sequence[int], tokens
         lp[i], tok[i], in_range = score_row(_get_row(logits, r), t, levels)
         ok = ok and in_range
     return out_off, lp, tok, ok
+
+
+def assemble(out_offsets, logprobs, token_ids, batch_top_n, vocab_size):
+    """Per-batch result objects from the output rows, as the MAX page's host step does
+    ("compute_top 的结果组装"): ``top_n == 0`` gives None; ``top_n`` outside
+    ``[0, W-1]`` is an error; each row's candidate columns (all but the last) drop
+    padding ids (>= vocab_size), are ordered by logprob descending and cut to
+    ``top_n``; the last column's (actual or sampled) token is then written into the
+    row's dict, replacing an equal key. Returns ``[None | (token_logprobs, top_dicts)]``.
+    """
+    W = logprobs.shape[1]
+    results = []
+    for b, top_n in enumerate(batch_top_n):
+        top_n = int(top_n)
+        if top_n < 0:
+            raise ValueError("top_n must be >= 0")
+        if top_n > W - 1:
+            raise ValueError("top_n exceeds the candidates kept per row; build with more levels")
+        if top_n == 0:
+            results.append(None)
+            continue
+        token_lps, tops = [], []
+        for o in range(int(out_offsets[b]), int(out_offsets[b + 1])):
+            pairs = [(int(token_ids[o, c]), float(logprobs[o, c])) for c in range(W - 1)
+                     if int(token_ids[o, c]) < vocab_size]
+            pairs = sorted(pairs, key=lambda p: -p[1])[:top_n]
+            d = dict(pairs)
+            d[int(token_ids[o, W - 1])] = float(logprobs[o, W - 1])
+            tops.append(d)
+            token_lps.append(float(logprobs[o, W - 1]))
+        results.append((token_lps, tops))
+    return results

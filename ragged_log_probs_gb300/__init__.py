@@ -18,10 +18,11 @@ from typing import Optional
 import torch
 
 from . import _build
+from .results import LogProbabilities, assemble  # noqa: F401  (host-side result assembly)
 
 __all__ = [
     "LpError", "lib_path", "load", "workspace_size", "new_workspace", "plan", "compute",
-    "read_status", "ragged_log_probs", "out_per_token", "STATUS_NAMES",
+    "read_status", "ragged_log_probs", "out_per_token", "STATUS_NAMES", "LogProbabilities", "assemble",
 ]
 
 LP_MAX_LEVELS = 6

@@ -56,3 +56,26 @@ def test_flashinfer_shape_grid(dist, B, V):
 def test_every_levels(levels):
     b = workloads.make_batch("mixed", "cuda", B=10, max_len=12, V=5003, levels=levels, seed=40 + levels)
     parity.check_batch(b)
+
+
+def test_host_assembly_from_gpu_rows():
+    # The user-facing result (MAX page, "compute_top 的结果组装") from the GPU rows vs the
+    # oracle's rows: per-batch None pattern, dict keys exact, values within tolerance.
+    import oracle
+    import ragged_log_probs_gb300 as lp
+    b = workloads.make_batch("mixed", "cuda", B=10, max_len=16)
+    out_off, out_lp, out_tok = lp.ragged_log_probs(b.logits, b.logit_row_offsets, b.tokens, b.sampled_tokens,
+                                                   b.echo, b.levels)
+    top_n = np.random.default_rng(3).integers(0, 8, size=b.B)
+    got = lp.assemble(out_off, out_lp, out_tok, top_n, b.V)
+    r_off, r_lp, r_tok, _ = parity.oracle_for(b)
+    want = oracle.assemble(r_off, r_lp, r_tok, top_n, b.V)
+    for g, w in zip(got, want):
+        if w is None:
+            assert g is None
+            continue
+        assert [set(d) for d in g.top_log_probabilities] == [set(d) for d in w[1]]
+        for dg, dw in zip(g.top_log_probabilities, w[1]):
+            for k in dw:
+                assert abs(dg[k] - dw[k]) <= 1e-4 or dg[k] == dw[k]
+        np.testing.assert_allclose(g.token_log_probabilities, w[0], atol=1e-4)

@@ -69,6 +69,23 @@ def _score_row_sign_flipped(x32, target, levels):
     return -lp, tok, ok
 
 
+def _assemble_without_forced_token(out_offsets, logprobs, token_ids, batch_top_n, vocab_size):
+    W = logprobs.shape[1]
+    res = []
+    for b, top_n in enumerate(batch_top_n):
+        if int(top_n) == 0:
+            res.append(None)
+            continue
+        tops, lps = [], []
+        for o in range(int(out_offsets[b]), int(out_offsets[b + 1])):
+            pairs = [(int(token_ids[o, c]), float(logprobs[o, c])) for c in range(W - 1)
+                     if int(token_ids[o, c]) < vocab_size]
+            tops.append(dict(sorted(pairs, key=lambda p: -p[1])[:int(top_n)]))
+            lps.append(float(logprobs[o, W - 1]))
+        res.append((lps, tops))
+    return res
+
+
 def _out_per_token_no_slot(levels):
     return 2 ** levels - 1 if levels > 0 else 1
 
@@ -84,6 +101,7 @@ MUTATIONS = {
     "echo_count_short": ("output_row_offsets", _offsets_short_count),
     "logprob_sign_flipped": ("score_row", _score_row_sign_flipped),
     "no_sampled_slot": ("out_per_token", _out_per_token_no_slot),
+    "assembly_drops_actual_token": ("assemble", _assemble_without_forced_token),
 }
 
 

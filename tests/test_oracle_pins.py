@@ -242,3 +242,26 @@ def test_invariants_on_tiny_workload():
     ties = np.flatnonzero(r0 == r0.max())
     assert len(ties) == 2
     assert tok[0, :2].tolist() == sorted(ties.tolist())
+
+
+def test_assemble_hand_example():
+    # MAX page, "compute_top 的结果组装": padding ids dropped, candidates ordered by logprob
+    # and cut to top_n, the last column's token forced in (replacing an equal key),
+    # top_n == 0 -> None, top_n outside [0, W-1] -> error. Worked by hand for W = 4.
+    PAD = oracle.PAD_ID
+    off = np.array([0, 2, 3])
+    tok = np.array([[5, 2, PAD, 7], [3, 4, 5, 3], [1, 2, 3, 9]], dtype=np.uint64)
+    lp = np.array([[-0.1, -1.0, -np.inf, -3.0], [-0.5, -0.7, -2.0, -0.5], [-0.2, -0.3, -4.0, -6.0]])
+    res = oracle.assemble(off, lp, tok, batch_top_n=[2, 0], vocab_size=10)
+    assert res[1] is None
+    token_lps, tops = res[0]
+    assert token_lps == [-3.0, -0.5]
+    assert tops[0] == {5: -0.1, 2: -1.0, 7: -3.0}
+    assert tops[1] == {3: -0.5, 4: -0.7}
+    res = oracle.assemble(off, lp, tok, batch_top_n=[1, 3], vocab_size=10)
+    assert res[0][1][1] == {3: -0.5}
+    assert res[1][1][0] == {1: -0.2, 2: -0.3, 3: -4.0, 9: -6.0}
+    with pytest.raises(ValueError):
+        oracle.assemble(off, lp, tok, batch_top_n=[4, 1], vocab_size=10)
+    with pytest.raises(ValueError):
+        oracle.assemble(off, lp, tok, batch_top_n=[-1, 1], vocab_size=10)
