@@ -48,9 +48,9 @@ WORKLOAD_TEXT = {
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 135671040, "source_hash": "20203a29c7034b56",
+    "decode": {"bytes_per_launch": 135530752, "source_hash": "46fbf212b89b4868",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 904610560, "source_hash": "20203a29c7034b56",
+    "prefill": {"bytes_per_launch": 904372224, "source_hash": "46fbf212b89b4868",
                 "capture": "profiles/k_rows_prefill.md"},
 }
 
