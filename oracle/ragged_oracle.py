@@ -31,7 +31,15 @@ Readings taken where the pages are silent (each is also listed in the design doc):
 * ``-inf`` logits are valid tokens with probability 0; a row of only ``-inf``
   has ``lse = NaN`` semantics (``-inf - -inf``), so all its logprobs are NaN.
 * A target token ``>= V`` gets logprob NaN and is reported as an error.
-* Raw logits, no temperature.
+* Raw logits unless per-batch temperatures are given. With temperature ``tau_b``
+  (the sampler's scaling on the SGLang page, "第二步：采样层选出 token_id，同时计算
+  logprob": the logprobs reuse the softmax taken after temperature scaling) the
+  values are ``x_v / tau_b - logsumexp(x / tau_b)``; the top-k ranking stays on the
+  raw fp32 logits, which is the same order because ``tau_b > 0``.
+* VARIABLE logits (MAX page, "echo 的前置条件：ReturnLogits 枚举"): when the input
+  positions are given separately, batch ``b``'s logits rows
+  ``[loff[b], loff[b+1])`` hold its LAST ``loff[b+1] - loff[b]`` positions, which
+  must cover the positions it scores.
 
 Every function here has a pin in ``tests/test_oracle_pins.py``.
 """
@@ -114,7 +122,8 @@ def output_row_offsets(logit_row_offsets: Sequence[int], echo: Sequence[bool]) -
 
 
 def output_rows(logit_row_offsets: Sequence[int], echo: Sequence[bool],
-                tokens: Sequence[int], sampled_tokens: Sequence[int]) -> list[tuple[int, int, int]]:
+                tokens: Sequence[int], sampled_tokens: Sequence[int],
+                input_row_offsets: Sequence[int] | None = None) -> list[tuple[int, int, int]]:
     """For every output row in order: ``(batch, logits_row, target_token)``.
 
     Echo batches emit one row per input position, non-echo batches one row for
@@ -122,22 +131,33 @@ def output_rows(logit_row_offsets: Sequence[int], echo: Sequence[bool],
     same sequence, and the last position scores the batch's sampled token.
     ("input logprob 和 output logprob 来自哪里" on the SGLang page; sampled-token
     slot in "compute_top 的结果组装" on the MAX page.)
+
+    With ``input_row_offsets`` (VARIABLE logits) positions and tokens follow those
+    offsets, and position ``p`` of batch ``b`` reads logits row
+    ``loff[b+1] - (ioff[b+1] - p)``: the present rows are the batch's last ones.
+    A batch whose present rows do not cover its scored positions is an error.
     """
-    off = [int(v) for v in logit_row_offsets]
+    loff = [int(v) for v in logit_row_offsets]
+    ioff = loff if input_row_offsets is None else [int(v) for v in input_row_offsets]
+    if len(ioff) != len(loff):
+        raise ValueError("input and logits offsets must both have B+1 entries")
     rows = []
-    for b in range(len(off) - 1):
-        start, end = off[b], off[b + 1]
+    for b in range(len(ioff) - 1):
+        start, end = ioff[b], ioff[b + 1]
         count = (end - start) if bool(echo[b]) else 1
+        present = loff[b + 1] - loff[b]
+        if present < count:
+            raise ValueError(f"batch {b} has {present} logits rows but scores {count} positions")
         for j in range(count):
-            r = end - count + j
-            t = int(tokens[r + 1]) if r + 1 < end else int(sampled_tokens[b])
-            rows.append((b, r, t))
+            p = end - count + j
+            t = int(tokens[p + 1]) if p + 1 < end else int(sampled_tokens[b])
+            rows.append((b, loff[b + 1] - (end - p), t))
     return rows
 
 
-def row_logsumexp(x32: np.ndarray) -> float:
-    """``log(sum(exp(x)))`` of one fp32 row, evaluated in fp64 with the max shift."""
-    x = np.asarray(x32, dtype=np.float64)
+def row_logsumexp(x32: np.ndarray, temperature: float = 1.0) -> float:
+    """``log(sum(exp(x / temperature)))`` of one fp32 row, in fp64 with the max shift."""
+    x = np.asarray(x32, dtype=np.float64) / np.float64(temperature)
     m = x.max()
     return float(m + np.log(np.sum(np.exp(x - m))))
 
@@ -162,13 +182,16 @@ def _get_row(logits: RowSource, r: int) -> np.ndarray:
     return np.asarray(logits[r], dtype=np.float32)
 
 
-def score_row(x32: np.ndarray, target: int, levels: int) -> tuple[np.ndarray, np.ndarray, bool]:
-    """One output row: ``W`` logprobs (fp64) and ids; flag says the target was in range."""
+def score_row(x32: np.ndarray, target: int, levels: int,
+              temperature: float = 1.0) -> tuple[np.ndarray, np.ndarray, bool]:
+    """One output row: ``W`` logprobs (fp64) and ids; flag says the target was in range.
+
+    Values are log-softmax of ``x / temperature``; ids rank the raw fp32 logits."""
     V = x32.shape[0]
     K = top_k_capacity(levels)
     W = out_per_token(levels)
-    x = np.asarray(x32, dtype=np.float64)
-    lse = row_logsumexp(x32)
+    x = np.asarray(x32, dtype=np.float64) / np.float64(temperature)
+    lse = row_logsumexp(x32, temperature)
     lp = np.empty(W, dtype=np.float64)
     tok = np.empty(W, dtype=np.uint64)
     if K > 0:
@@ -184,10 +207,14 @@ def score_row(x32: np.ndarray, target: int, levels: int) -> tuple[np.ndarray, np
 
 def ragged_log_probs(logits: RowSource, logit_row_offsets: Sequence[int], tokens: Sequence[int],
                      sampled_tokens: Sequence[int], echo: Sequence[bool], levels: int,
-                     rows: Sequence[int] | None = None, T: int | None = None):
+                     rows: Sequence[int] | None = None, T: int | None = None,
+                     temperatures: Sequence[float] | None = None,
+                     input_row_offsets: Sequence[int] | None = None):
     """Reference result of the whole path.
 
     ``logits`` is a 2-D fp32 array ``[T, V]`` or a callable ``r -> row``.
+    ``temperatures`` (one positive value per batch) scales the logits before the
+    softmax; ``input_row_offsets`` switches to VARIABLE logits (see ``output_rows``).
     Returns ``(out_offsets u64[B+1], logprobs f64[R', W], token_ids u64[R', W],
     all_targets_in_range)`` where ``R'`` is every output row, or only ``rows``
     (output-row indices) when given.
@@ -195,18 +222,30 @@ def ragged_log_probs(logits: RowSource, logit_row_offsets: Sequence[int], tokens
     if T is None:
         T = int(logits.shape[0]) if not callable(logits) else int(logit_row_offsets[-1])
     validate_offsets(logit_row_offsets, T)
+    pos_off = logit_row_offsets
+    if input_row_offsets is not None:
+        validate_offsets(input_row_offsets, int(input_row_offsets[-1]))
+        pos_off = input_row_offsets
     if levels < 0:
         raise ValueError("levels must be >= 0")
-    out_off = output_row_offsets(logit_row_offsets, echo)
-    mapping = output_rows(logit_row_offsets, echo, tokens, sampled_tokens)
+    B = len(pos_off) - 1
+    if temperatures is not None:
+        if len(temperatures) != B:
+            raise ValueError("one temperature per batch")
+        for tau in temperatures:
+            if not (math.isfinite(float(tau)) and float(tau) > 0.0):
+                raise ValueError("temperatures must be finite and > 0")
+    out_off = output_row_offsets(pos_off, echo)
+    mapping = output_rows(logit_row_offsets, echo, tokens, sampled_tokens, input_row_offsets)
     wanted = range(len(mapping)) if rows is None else [int(o) for o in rows]
     W = out_per_token(levels)
     lp = np.empty((len(wanted), W), dtype=np.float64)
     tok = np.empty((len(wanted), W), dtype=np.uint64)
     ok = True
     for i, o in enumerate(wanted):
-        _, r, t = mapping[o]
-        lp[i], tok[i], in_range = score_row(_get_row(logits, r), t, levels)
+        b, r, t = mapping[o]
+        tau = 1.0 if temperatures is None else float(temperatures[b])
+        lp[i], tok[i], in_range = score_row(_get_row(logits, r), t, levels, tau)
         ok = ok and in_range
     return out_off, lp, tok, ok
 

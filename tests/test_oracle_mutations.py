@@ -86,11 +86,34 @@ def _assemble_without_forced_token(out_offsets, logprobs, token_ids, batch_top_n
     return res
 
 
+def _score_row_multiplies_temperature(x32, target, levels, temperature=1.0):
+    return _orig_score_row(x32, target, levels, 1.0 / temperature)
+
+
+def _score_row_lse_unscaled(x32, target, levels, temperature=1.0):
+    lp, tok, ok = _orig_score_row(x32, target, levels, temperature)
+    shift = ro.row_logsumexp(x32, temperature) - ro.row_logsumexp(x32, 1.0)
+    return lp + shift, tok, ok
+
+
+def _rows_variable_reads_first_present(logit_row_offsets, echo, tokens, sampled, input_row_offsets=None):
+    rows = _orig_output_rows(logit_row_offsets, echo, tokens, sampled, input_row_offsets)
+    if input_row_offsets is None:
+        return rows
+    out, j, prev = [], 0, None
+    for (b, r, t) in rows:
+        j = j + 1 if b == prev else 0
+        prev = b
+        out.append((b, int(logit_row_offsets[b]) + j, t))
+    return out
+
+
 def _out_per_token_no_slot(levels):
     return 2 ** levels - 1 if levels > 0 else 1
 
 
 _orig_score_row = ro.score_row
+_orig_output_rows = ro.output_rows
 
 MUTATIONS = {
     "lse_drops_log": ("row_logsumexp", _lse_without_log),
@@ -102,6 +125,9 @@ MUTATIONS = {
     "logprob_sign_flipped": ("score_row", _score_row_sign_flipped),
     "no_sampled_slot": ("out_per_token", _out_per_token_no_slot),
     "assembly_drops_actual_token": ("assemble", _assemble_without_forced_token),
+    "temperature_multiplies": ("score_row", _score_row_multiplies_temperature),
+    "temperature_lse_unscaled": ("score_row", _score_row_lse_unscaled),
+    "variable_reads_first_present_rows": ("output_rows", _rows_variable_reads_first_present),
 }
 
 

@@ -265,3 +265,111 @@ def test_assemble_hand_example():
         oracle.assemble(off, lp, tok, batch_top_n=[4, 1], vocab_size=10)
     with pytest.raises(ValueError):
         oracle.assemble(off, lp, tok, batch_top_n=[-1, 1], vocab_size=10)
+
+
+# --- temperature (SGLang page: the sampler's softmax after temperature scaling) ---------
+
+def _one_row(x, target, levels, tau):
+    off, lp, tok, ok = oracle.ragged_log_probs(np.asarray(x, dtype=np.float32)[None, :], [0, 1], [0], [target],
+                                               [False], levels, temperatures=[tau])
+    return lp[0], tok[0], ok
+
+
+def test_temperature_two_token_closed_form():
+    # Two logits a > b at temperature tau: p(a) = 1 / (1 + e^{(b - a)/tau}), the logistic
+    # function, so log p(a) = -log1p(e^{(b-a)/tau}) and log p(b) = -log1p(e^{(a-b)/tau}).
+    a, b = 1.75, -0.5
+    for tau in (0.25, 0.5, 1.0, 2.0, 3.0, 10.0):
+        lp, tok, ok = _one_row([b, a], target=0, levels=1, tau=tau)
+        assert ok and tok.tolist() == [1, 0]
+        assert abs(lp[0] - (-math.log1p(math.exp((b - a) / tau)))) < 1e-14
+        assert abs(lp[1] - (-math.log1p(math.exp((a - b) / tau)))) < 1e-14
+
+
+def test_temperature_matches_scipy_of_scaled_row():
+    rng = np.random.default_rng(21)
+    for V, tau in ((50, 0.6), (63, 1.7), (200, 0.05)):
+        x = (rng.standard_normal(V) * 3).astype(np.float32)
+        ref = scipy.special.log_softmax(x.astype(np.float64) / tau)
+        lp, tok, _ = _one_row(x, target=V - 1, levels=6, tau=tau)
+        for c in range(63):
+            if tok[c] != PAD_ID:
+                assert abs(lp[c] - ref[int(tok[c])]) < 1e-11
+        assert abs(lp[63] - ref[V - 1]) < 1e-11
+
+
+def test_temperature_limits():
+    rng = np.random.default_rng(22)
+    V = 100
+    x = (rng.standard_normal(V) * 2).astype(np.float32)
+    # tau -> infinity: the distribution flattens to uniform, every logprob -> -log V
+    lp, _, _ = _one_row(x, target=3, levels=3, tau=1e7)
+    np.testing.assert_allclose(lp, -math.log(V), atol=1e-5, rtol=0)
+    # tau -> 0: all mass on the largest logit (gap to the runner-up >= 0.05 here)
+    x[7] = x.max() + 0.25
+    lp, tok, _ = _one_row(x, target=3, levels=3, tau=1e-3)
+    assert tok[0] == 7 and lp[0] > -1e-15 and lp[1] < -40
+
+
+def test_temperature_keeps_ids_and_one_is_plain():
+    import workloads
+    b = workloads.make_batch("tiny", "cpu")
+    off, tok_in, sampled, echo = b.host()
+    x = b.logits.numpy()
+    plain = oracle.ragged_log_probs(x, off, tok_in, sampled, echo, b.levels)
+    ones = oracle.ragged_log_probs(x, off, tok_in, sampled, echo, b.levels, temperatures=[1.0] * b.B)
+    assert np.array_equal(plain[1], ones[1]) and np.array_equal(plain[2], ones[2])
+    for taus in ([0.3, 2.0, 7.0, 0.9], [5.0] * 4):
+        hot = oracle.ragged_log_probs(x, off, tok_in, sampled, echo, b.levels, temperatures=taus)
+        assert np.array_equal(hot[2], plain[2])          # ids rank the raw logits
+        for o in range(hot[1].shape[0]):
+            # each row stays a log-distribution: top-k + rest sums to at most 1
+            assert scipy.special.logsumexp(hot[1][o, :7]) <= 1e-12
+
+
+def test_temperature_rejects_non_positive():
+    x = np.zeros((1, 4), dtype=np.float32)
+    for tau in (0.0, -1.0, math.nan, math.inf):
+        with pytest.raises(ValueError):
+            oracle.ragged_log_probs(x, [0, 1], [0], [0], [False], 1, temperatures=[tau])
+
+
+# --- VARIABLE logits (MAX page: "echo 的前置条件：ReturnLogits 枚举") ---------------------
+
+def test_variable_hand_mapping():
+    # Tiny layout, lengths {3,5,1,7}, echo {T,F,T,F}; logits present for the last
+    # {3,2,1,1} positions of each sequence, so loff = [0,3,5,6,7]. Worked by hand:
+    # batch 0 scores positions 0,1,2 from logits rows 0,1,2 (targets tokens[1], tokens[2],
+    # sampled[0]); batch 1 scores its last position 7 from row 4 (its last present row);
+    # batch 2 position 8 from row 5; batch 3 position 15 from row 6.
+    ioff = [0, 3, 8, 9, 16]
+    loff = [0, 3, 5, 6, 7]
+    tokens = list(range(100, 116))
+    sampled = [900, 901, 902, 903]
+    rows = oracle.output_rows(loff, [True, False, True, False], tokens, sampled, input_row_offsets=ioff)
+    assert rows == [(0, 0, 101), (0, 1, 102), (0, 2, 900), (1, 4, 901), (2, 5, 902), (3, 6, 903)]
+    assert oracle.output_row_offsets(ioff, [True, False, True, False]).tolist() == [0, 3, 4, 5, 6]
+
+
+def test_variable_equals_all_mode_on_gathered_rows():
+    import workloads
+    b = workloads.make_batch("tiny", "cpu")
+    off, tok_in, sampled, echo = b.host()
+    x = b.logits.numpy()
+    full = oracle.ragged_log_probs(x, off, tok_in, sampled, echo, b.levels)
+    # same offsets for both: VARIABLE with every position present is ALL mode
+    same = oracle.ragged_log_probs(x, off, tok_in, sampled, echo, b.levels, input_row_offsets=off)
+    assert np.array_equal(full[1], same[1]) and np.array_equal(full[2], same[2])
+    # keep only the rows the output needs (hand-listed for lengths {3,5,1,7}, echo {T,F,T,F})
+    keep = [0, 1, 2, 7, 8, 15]
+    compact = oracle.ragged_log_probs(x[keep], [0, 3, 4, 5, 6], tok_in, sampled, echo, b.levels,
+                                      input_row_offsets=off)
+    assert np.array_equal(full[0], compact[0])
+    assert np.array_equal(full[1], compact[1]) and np.array_equal(full[2], compact[2])
+
+
+def test_variable_too_few_rows_rejected():
+    x = np.zeros((4, 8), dtype=np.float32)
+    with pytest.raises(ValueError):   # echo batch of 3 positions with 2 logits rows
+        oracle.ragged_log_probs(x, [0, 2, 4], list(range(5)), [0, 0], [True, False], 1,
+                                input_row_offsets=[0, 3, 5])
