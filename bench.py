@@ -44,6 +44,21 @@ WORKLOAD_TEXT = {
     "wide": "wide top-k: B=32, lengths U[128,1024], V=256000, levels=6, all echo, N(0,1) quantised to 1/16",
 }
 
+VARIANT_TEXT = {
+    "none": "",
+    "temperature": "; per-batch temperatures U[0.25,2] (every 4th exactly 1), logprobs of x/tau",
+    "variable": "; VARIABLE logits: only each sequence's last positions present (all for echo, 1-3 otherwise)",
+}
+
+
+def load_batch(config: str, variant: str, dev):
+    import workloads
+    batch = workloads.make_batch(config, dev, variable_extra=2 if variant == "variable" else None)
+    if variant == "temperature":
+        batch = workloads.with_temperatures(batch, seed=11)
+    return batch
+
+
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the row kernel,
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
@@ -165,8 +180,8 @@ def whole_job_rows_per_s(rows_per_rank: int, world: int, ms_per_step: float) -> 
 # ------------------------------------------------------------------------ oracle leg
 def _oracle_row(args):
     import oracle
-    row, t, levels = args
-    return oracle.score_row(row, t, levels)[0][0]
+    row, t, levels, tau = args
+    return oracle.score_row(row, t, levels, tau)[0][0]
 
 
 def cpu_cores() -> int:
@@ -182,16 +197,17 @@ def oracle_sample(batch, n_rows: int, seed: int = 0):
     import numpy as np
     import oracle
     off, tokens, sampled, echo = batch.host()
-    mapping = oracle.output_rows(off, echo, tokens, sampled)
+    ioff, tau = batch.host_variant()
+    mapping = oracle.output_rows(off, echo, tokens, sampled, input_row_offsets=ioff)
     rng = np.random.default_rng(seed)
     picks = rng.choice(len(mapping), size=n_rows, replace=n_rows > len(mapping))
     cache = {}
     items = []
     for o in picks:
-        r = mapping[o][1]
+        b, r, t = mapping[o]
         if r not in cache:
             cache[r] = batch.logits[r].cpu().numpy()
-        items.append((cache[r], mapping[o][2], batch.levels))
+        items.append((cache[r], t, batch.levels, 1.0 if tau is None else float(tau[b])))
     return items
 
 
@@ -222,12 +238,15 @@ def run_ours(args, rank: int, world: int, dist):
     _build.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    batch = workloads.make_batch(args.config, dev)
-    B, T, V, levels = batch.B, batch.T, batch.V, batch.levels
+    batch = load_batch(args.config, args.variant, dev)
+    B, T_logits, V, levels = batch.B, batch.T, batch.V, batch.levels
+    T = batch.tokens.numel()  # input positions (== T_logits unless VARIABLE logits)
+    pos_off = batch.positions_offsets
+    extended = args.variant != "none"
     W = lp.out_per_token(levels)
     ws = lp.new_workspace(B, T, V, levels, dev)
     host = torch.zeros(2, dtype=torch.int32).pin_memory()
-    out_off = lp.plan(batch.logit_row_offsets, batch.echo, T, ws, host_out=host)
+    out_off = lp.plan(pos_off, batch.echo, T, ws, host_out=host)
     torch.cuda.synchronize()
     R = int(host[0])
     if int(host[1]) != 0:
@@ -243,12 +262,19 @@ def run_ours(args, rank: int, world: int, dist):
     copies = [batch.logits] + [batch.logits.clone() for _ in range(n_copies - 1)]
     stream = torch.cuda.current_stream()
 
+    def launch_compute(logits, loff, ioff, tokens, sampled, echo, tau):
+        if extended:
+            lp.compute_ex(logits, loff, tokens, sampled, out_off, echo, levels, out_lp, out_tok, ws,
+                          input_row_offsets=ioff, temperatures=tau, stream=stream)
+        else:
+            lp.compute(logits, loff, tokens, sampled, out_off, echo, levels, out_lp, out_tok, ws, stream=stream)
+
     def step(i, ev=None):
-        lp.plan(batch.logit_row_offsets, batch.echo, T, ws, output_row_offsets=out_off, stream=stream)
+        lp.plan(pos_off, batch.echo, T, ws, output_row_offsets=out_off, stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        lp.compute(copies[i % n_copies], batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, out_off,
-                   batch.echo, levels, out_lp, out_tok, ws, stream=stream)
+        launch_compute(copies[i % n_copies], batch.logit_row_offsets, batch.input_row_offsets, batch.tokens,
+                       batch.sampled_tokens, batch.echo, batch.temperatures)
         if ev is not None:
             ev[1].record(stream)
 
@@ -318,11 +344,14 @@ def run_ours(args, rank: int, world: int, dist):
     e2e = None
     if not args.no_e2e:
         h_logits = batch.logits.cpu().pin_memory()
-        h_ints = [t.cpu().pin_memory() for t in (batch.logit_row_offsets, batch.tokens, batch.sampled_tokens,
-                                                  batch.echo)]
+        # logits offsets, tokens, sampled, echo, then the variant's inputs (input offsets, temperatures)
+        small = [batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, batch.echo]
+        small += [t for t in (batch.input_row_offsets, batch.temperatures) if t is not None]
+        h_ints = [t.cpu().pin_memory() for t in small]
         d_logits = torch.empty_like(batch.logits)
-        d_ints = [torch.empty_like(t) for t in (batch.logit_row_offsets, batch.tokens, batch.sampled_tokens,
-                                                batch.echo)]
+        d_ints = [torch.empty_like(t) for t in small]
+        d_ioff = d_ints[4] if batch.input_row_offsets is not None else None
+        d_tau = d_ints[-1] if batch.temperatures is not None else None
         h_lp = torch.empty((R, W), dtype=torch.float32).pin_memory()
         h_tok = torch.empty((R, W), dtype=torch.int32).pin_memory()
         h2d = h_logits.numel() * 4 + sum(t.numel() * t.element_size() for t in h_ints)
@@ -333,9 +362,9 @@ def run_ours(args, rank: int, world: int, dist):
             d_logits.copy_(h_logits, non_blocking=True)
             for d, h in zip(d_ints, h_ints):
                 d.copy_(h, non_blocking=True)
-            lp.plan(d_ints[0], d_ints[3], T, ws, output_row_offsets=out_off, stream=stream)
-            lp.compute(d_logits, d_ints[0], d_ints[1], d_ints[2], out_off, d_ints[3], levels, out_lp, out_tok, ws,
-                       stream=stream)
+            lp.plan(d_ioff if d_ioff is not None else d_ints[0], d_ints[3], T, ws, output_row_offsets=out_off,
+                    stream=stream)
+            launch_compute(d_logits, d_ints[0], d_ioff, d_ints[1], d_ints[2], d_ints[3], d_tau)
             h_lp.copy_(out_lp, non_blocking=True)
             h_tok.copy_(out_tok, non_blocking=True)
 
@@ -369,11 +398,12 @@ def run_ours(args, rank: int, world: int, dist):
     achieved = alg / (compute_ms / 1e3) / 1e9
     peak, peak_src = measured_peak_hbm()
     traffic = None
-    rec = NCU_TRAFFIC.get(args.config)
+    rec = NCU_TRAFFIC.get(args.config if args.variant == "none" else f"{args.config}/{args.variant}")
     if rec and rec.get("source_hash") == kernel_source_hash():
         traffic = rec["bytes_per_launch"]
-    kernel_name = ("k_rows_cta (lp_ragged_compute, row queue)" if 2 * T < rows_kernel_warps()
-                   else "k_rows (lp_ragged_compute, warp ranges)")
+    entry = "lp_ragged_compute_ex" if extended else "lp_ragged_compute"
+    kernel_name = (f"k_rows_cta ({entry}, row queue)" if 2 * min(T, T_logits) < rows_kernel_warps()
+                   else f"k_rows ({entry}, warp ranges)")
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                 "timing": f"CUDA events around each of {n_ev} compute launches, same stream, right after the timed steps",
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -395,7 +425,8 @@ def run_ours(args, rank: int, world: int, dist):
         "metric": METRIC, "value": whole_job_rows_per_s(R, world, ms_step), "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "B": B, "T": T, "V": V,
+        "config": {"workload": WORKLOAD_TEXT[args.config] + VARIANT_TEXT[args.variant], "name": args.config,
+                   "variant": args.variant, "B": B, "T": T, "T_logits": T_logits, "V": V,
                    "levels": levels, "rows_per_gpu": R, "parallelism": f"replicas x{world} (independent batches)",
                    "l2": f"inputs larger than L2: {n_copies} rotating logits copies of {lbytes / 1e6:.0f} MB "
                          f"(L2 {l2 / 1e6:.0f} MB)"},
@@ -419,7 +450,7 @@ def run_reference(args, rank: int, world: int):
     cores = cpu_cores()
     with mp.get_context("spawn").Pool(cores) as pool:
         dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-        batch = workloads.make_batch(args.config, dev)
+        batch = load_batch(args.config, args.variant, dev)
         probe = oracle_sample(batch, 1, seed=99)
         t = time.perf_counter()
         _oracle_row(probe[0])
@@ -444,7 +475,8 @@ def run_reference(args, rank: int, world: int):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "B": batch.B, "T": batch.T,
+        "config": {"workload": WORKLOAD_TEXT[args.config] + VARIANT_TEXT[args.variant], "name": args.config,
+                   "variant": args.variant, "B": batch.B, "T": batch.tokens.numel(), "T_logits": batch.T,
                    "V": batch.V, "levels": batch.levels},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -459,6 +491,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="decode", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--variant", default="none", choices=sorted(VARIANT_TEXT),
+                    help="input variant: per-batch temperature or VARIABLE logits (lp_ragged_compute_ex)")
     ap.add_argument("--settle-s", type=float, default=1.0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -55,7 +55,8 @@ typedef enum lp_status {
                                 output offsets that disagree with the echo flags           */
     LP_ERR_TOKEN_RANGE = 5,  /* device: an actual or sampled token >= V                     */
     LP_ERR_WORKSPACE = 6,    /* workspace NULL or smaller than lp_ragged_workspace_size     */
-    LP_ERR_CUDA = 7          /* a CUDA launch or copy failed                                */
+    LP_ERR_CUDA = 7,         /* a CUDA launch or copy failed                                */
+    LP_ERR_TEMPERATURE = 8   /* device: a temperature that is not a positive finite number  */
 } lp_status;
 
 #define LP_MAX_LEVELS 6u
@@ -115,6 +116,47 @@ lp_status lp_ragged_compute(const float *logits, uint32_t T, uint32_t V,
                             const uint32_t *output_row_offsets, const uint8_t *echo, uint32_t levels,
                             float *out_logprobs, uint32_t *out_tokens,
                             void *workspace, size_t workspace_bytes, lp_stream_t stream);
+
+/*
+ * Step 2, extended: the same reduction for two variants of the caller's input.
+ *
+ * VARIABLE logits ("MAX Python SDK 中 log_probabilities 模块解析", section "echo 的
+ * 前置条件：ReturnLogits 枚举": the model returns logits for only some positions).
+ * Positions and logits rows are described separately:
+ *   input_row_offsets   device, uint32[B+1]: batch b's positions [ioff[b], ioff[b+1])
+ *                       of the T flat tokens; the output layout (plan) follows these.
+ *   logit_row_offsets   device, uint32[B+1]: batch b's rows [loff[b], loff[b+1]) of
+ *                       the T_logits logits rows, holding the LAST loff[b+1]-loff[b]
+ *                       positions of the sequence. They must cover the positions the
+ *                       batch scores (all of them with echo, the last one without);
+ *                       otherwise the batch's rows get NaN / 0xFFFFFFFF and the
+ *                       LP_ERR_OFFSETS bit is set.
+ *   input_row_offsets == NULL means every position has its logits row (T == T_logits
+ *   required, else LP_ERR_SHAPE), which is lp_ragged_compute.
+ *   Call lp_ragged_plan with input_row_offsets and T first.
+ *
+ * Temperature (SGLang page "logprob、finish reason 与 output processing", section
+ * "第二步：采样层选出 token_id，同时计算 logprob": the sampler scales the logits by
+ * the request's temperature and the logprobs reuse that softmax):
+ *   temperatures        device, float[B], or NULL for raw logits (tau = 1). Batch b's
+ *                       logprobs are those of x / tau_b: column c holds
+ *                       x[r, id] / tau_b - log(sum_v exp(x[r, v] / tau_b)). The top-K
+ *                       ids still rank the raw fp32 logits (the same order for
+ *                       tau_b > 0, and the ids stay exact). tau_b must be positive and
+ *                       finite, else the batch's rows get NaN / 0xFFFFFFFF and the
+ *                       LP_ERR_TEMPERATURE bit is set. Logits with |x| / tau beyond
+ *                       ~8.8e37 overflow the fp32 sum and give unspecified values.
+ *
+ * Other arguments, outputs, workspace and checks: as lp_ragged_compute, with
+ * logits float[T_logits][V] and tokens uint32[T].
+ */
+lp_status lp_ragged_compute_ex(const float *logits, uint32_t T_logits, uint32_t V,
+                               const uint32_t *logit_row_offsets, const uint32_t *input_row_offsets, uint32_t T,
+                               uint32_t B, const uint32_t *tokens, const uint32_t *sampled_tokens,
+                               const uint32_t *output_row_offsets, const uint8_t *echo,
+                               const float *temperatures, uint32_t levels, float *out_logprobs,
+                               uint32_t *out_tokens, void *workspace, size_t workspace_bytes,
+                               lp_stream_t stream);
 
 /*
  * Allocation-free form of lp_ragged_compute (no counterpart on the pages; it exists

@@ -22,16 +22,16 @@ from .results import LogProbabilities, assemble  # noqa: F401  (host-side result
 
 __all__ = [
     "LpError", "lib_path", "load", "workspace_size", "new_workspace", "plan", "compute",
-    "read_status", "ragged_log_probs", "out_per_token", "STATUS_NAMES", "LogProbabilities", "assemble",
+    "compute_ex", "read_status", "ragged_log_probs", "out_per_token", "STATUS_NAMES", "LogProbabilities", "assemble",
 ]
 
 LP_MAX_LEVELS = 6
 PAD_TOKEN = 0xFFFFFFFF
 STATUS_NAMES = {
     0: "LP_OK", 1: "LP_ERR_NULL", 2: "LP_ERR_LEVELS", 3: "LP_ERR_SHAPE", 4: "LP_ERR_OFFSETS",
-    5: "LP_ERR_TOKEN_RANGE", 6: "LP_ERR_WORKSPACE", 7: "LP_ERR_CUDA",
+    5: "LP_ERR_TOKEN_RANGE", 6: "LP_ERR_WORKSPACE", 7: "LP_ERR_CUDA", 8: "LP_ERR_TEMPERATURE",
 }
-EXPORTS = ("lp_ragged_workspace_size", "lp_ragged_plan", "lp_ragged_compute",
+EXPORTS = ("lp_ragged_workspace_size", "lp_ragged_plan", "lp_ragged_compute", "lp_ragged_compute_ex",
            "lp_ragged_read_status", "lp_ragged_strerror")
 
 
@@ -64,6 +64,8 @@ def load() -> ctypes.CDLL:
     lib.lp_ragged_plan.restype = ctypes.c_int
     lib.lp_ragged_compute.argtypes = [vp, u32, u32, vp, u32, vp, vp, vp, vp, u32, vp, vp, vp, sz, vp]
     lib.lp_ragged_compute.restype = ctypes.c_int
+    lib.lp_ragged_compute_ex.argtypes = [vp, u32, u32, vp, vp, u32, u32, vp, vp, vp, vp, vp, u32, vp, vp, vp, sz, vp]
+    lib.lp_ragged_compute_ex.restype = ctypes.c_int
     lib.lp_ragged_read_status.argtypes = [vp, vp, vp]
     lib.lp_ragged_read_status.restype = ctypes.c_int
     lib.lp_ragged_strerror.argtypes = [ctypes.c_int]
@@ -174,6 +176,45 @@ def compute(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: torch
         raise LpError(rc, "lp_ragged_compute")
 
 
+def compute_ex(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: torch.Tensor,
+               sampled_tokens: torch.Tensor, output_row_offsets: torch.Tensor, echo: torch.Tensor, levels: int,
+               out_logprobs: torch.Tensor, out_tokens: torch.Tensor, workspace: torch.Tensor,
+               input_row_offsets: Optional[torch.Tensor] = None, temperatures: Optional[torch.Tensor] = None,
+               stream=None) -> None:
+    """Enqueue ``lp_ragged_compute_ex``: VARIABLE logits (``input_row_offsets`` gives the
+    positions, ``logit_row_offsets`` the rows present in ``logits``, each batch's last
+    positions) and/or per-batch ``temperatures`` (float32 [B])."""
+    lib = load()
+    if logits.dim() != 2 or logits.dtype != torch.float32 or not logits.is_cuda:
+        raise TypeError("logits must be a 2-D float32 CUDA tensor")
+    if logits.stride(1) != 1 or logits.stride(0) != logits.shape[1]:
+        raise ValueError("logits must be row-major contiguous")
+    T_logits, V = logits.shape
+    B = logit_row_offsets.numel() - 1
+    T = tokens.numel()
+    ioff = 0
+    if input_row_offsets is not None:
+        ioff = _dev_u32(input_row_offsets, "input_row_offsets", B + 1)
+    elif T != T_logits:
+        raise ValueError("without input_row_offsets every position needs a logits row (tokens and logits rows)")
+    tp = 0
+    if temperatures is not None:
+        if temperatures.dtype != torch.float32 or not temperatures.is_cuda or not temperatures.is_contiguous() \
+                or temperatures.numel() < B:
+            raise TypeError("temperatures must be a contiguous float32 CUDA tensor with B entries")
+        tp = temperatures.data_ptr()
+    if out_logprobs.dtype != torch.float32 or not out_logprobs.is_cuda or not out_logprobs.is_contiguous():
+        raise TypeError("out_logprobs must be a contiguous float32 CUDA tensor")
+    rc = lib.lp_ragged_compute_ex(
+        logits.data_ptr(), T_logits, V, _dev_u32(logit_row_offsets, "logit_row_offsets", B + 1), ioff, T, B,
+        _dev_u32(tokens, "tokens", T), _dev_u32(sampled_tokens, "sampled_tokens", B),
+        _dev_u32(output_row_offsets, "output_row_offsets", B + 1), _dev_u8(echo, "echo", B), tp, levels,
+        out_logprobs.data_ptr(), _dev_u32(out_tokens, "out_tokens"),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc:
+        raise LpError(rc, "lp_ragged_compute_ex")
+
+
 def read_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronously read the device status bits (bit c set <=> error code c seen)."""
     lib = load()
@@ -187,16 +228,23 @@ def read_status(workspace: torch.Tensor, stream=None) -> int:
 
 def ragged_log_probs(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: torch.Tensor,
                      sampled_tokens: torch.Tensor, echo: torch.Tensor, levels: int,
-                     workspace: Optional[torch.Tensor] = None, stream=None, check: bool = True):
+                     workspace: Optional[torch.Tensor] = None, stream=None, check: bool = True,
+                     input_row_offsets: Optional[torch.Tensor] = None,
+                     temperatures: Optional[torch.Tensor] = None):
     """plan -> size outputs (one host sync for R) -> compute.
 
+    With ``input_row_offsets`` (VARIABLE logits) and/or ``temperatures`` the compute
+    step is ``lp_ragged_compute_ex``.
     Returns ``(output_row_offsets [B+1], logprobs f32 [R, W], token_ids int32-storage-of-uint32 [R, W])``."""
-    T, V = logits.shape
+    T_logits, V = logits.shape
     B = logit_row_offsets.numel() - 1
+    extended = input_row_offsets is not None or temperatures is not None
+    T = tokens.numel() if input_row_offsets is not None else T_logits
+    pos_off = input_row_offsets if input_row_offsets is not None else logit_row_offsets
     if workspace is None:
         workspace = new_workspace(B, T, V, levels, logits.device)
     host = torch.zeros(2, dtype=torch.int32).pin_memory()
-    out_off = plan(logit_row_offsets, echo, T, workspace, host_out=host, stream=stream)
+    out_off = plan(pos_off, echo, T, workspace, host_out=host, stream=stream)
     (torch.cuda.current_stream() if stream is None else stream).synchronize()
     R, status = int(host[0]), int(host[1]) & 0xFFFFFFFF
     if status:
@@ -204,8 +252,12 @@ def ragged_log_probs(logits: torch.Tensor, logit_row_offsets: torch.Tensor, toke
     W = out_per_token(levels)
     out_lp = torch.empty((R, W), dtype=torch.float32, device=logits.device)
     out_tok = torch.empty((R, W), dtype=torch.int32, device=logits.device)
-    compute(logits, logit_row_offsets, tokens, sampled_tokens, out_off, echo, levels, out_lp, out_tok,
-            workspace, stream=stream)
+    if extended:
+        compute_ex(logits, logit_row_offsets, tokens, sampled_tokens, out_off, echo, levels, out_lp, out_tok,
+                   workspace, input_row_offsets=input_row_offsets, temperatures=temperatures, stream=stream)
+    else:
+        compute(logits, logit_row_offsets, tokens, sampled_tokens, out_off, echo, levels, out_lp, out_tok,
+                workspace, stream=stream)
     if check:
         status = read_status(workspace, stream)
         if status:

@@ -17,10 +17,13 @@
 // takes a ticket; the warp that takes the last ticket merges the pieces and writes
 // the row. Nothing waits on another warp, so there is no inter-warp spin.
 //
-// Sum-exp in the log2 domain. A lane keeps m (largest logit seen), c = m*log2(e)
-// rounded to fp32, and s = sum 2^(x*log2(e) - c): one FFMA, one EX2 and one FADD per
-// logit. Then lse = c*ln2 + ln(s) (evaluated in fp64); the only approximation beyond
-// rounding is the fp32 value of log2(e), which scales the logits by 1 - 1.3e-8.
+// Sum-exp in the log2 domain. A lane keeps m (largest logit seen), c = m*k rounded to
+// fp32 with k = log2(e)/tau (tau = 1 unless a temperature is given), and
+// s = sum 2^(x*k - c): one FFMA, one EX2 and one FADD per logit. A logprob is then
+// (x*k - c)*ln2 - ln(s), formed in fp64 from the same fp32 k, so it is the exact
+// log-softmax of logits scaled by (1 + d)/tau, |d| <= 2^-24 (the rounding of k): the
+// error is |d| times the logit's distance from the softmax-weighted mean, below
+// 2^-24 * |logprob|.
 #pragma once
 
 #include <cstdint>
@@ -57,6 +60,7 @@ constexpr uint32_t kThrEvery = 4;  // blocks between lane-maximum threshold refr
 constexpr int kPlanThreads = 1024;
 constexpr uint32_t kStatusOffsets = 1u << 4;     // bit of LP_ERR_OFFSETS
 constexpr uint32_t kStatusTokenRange = 1u << 5;  // bit of LP_ERR_TOKEN_RANGE
+constexpr uint32_t kStatusTemperature = 1u << 8; // bit of LP_ERR_TEMPERATURE
 constexpr double kLn2 = 0.69314718055994530942;
 
 // Workspace: [header 256 B][arrival counters u32 x max warps, zeroed by plan, padded
@@ -76,7 +80,7 @@ __host__ __device__ inline uint32_t partial_stride_bytes(uint32_t K) {
 
 struct RowsParams {
     const float* logits;
-    const uint32_t* off;
+    const uint32_t* off;     // input positions (and tokens) per batch
     const uint32_t* tokens;
     const uint32_t* sampled;
     const uint32_t* out_off;
@@ -92,6 +96,12 @@ struct RowsParams {
     uint32_t min_piece;      // minimum vectors per warp
     uint32_t stage_offsets;  // 1: copy off / out_off / echo to shared memory
     uint32_t num_sms;        // SMs of the device (row-queue kernel: rows per SM cap)
+    // Extended inputs (read only by the EXT instantiations; kept last so the fields above
+    // keep their parameter offsets):
+    uint32_t T_logits;       // rows of logits
+    const uint32_t* loff;    // logits rows per batch: the batch's last positions (== off
+                             // when every position has a logits row)
+    const float* tau;        // per-batch temperature, or nullptr for raw logits
 };
 
 // ---------------------------------------------------------------------------------
@@ -161,18 +171,19 @@ __device__ __forceinline__ uint64_t sk_owner(uint64_t v, uint64_t Q, uint64_t G)
 // Per-lane running sum in the log2 domain.
 struct LaneSum {
     float m;  // largest logit seen (-inf: none)
-    float c;  // reference, m * log2(e) rounded (0 while m is -inf)
-    float s;  // sum of 2^(x * log2(e) - c)
-    __device__ __forceinline__ void init() { m = neg_inf(); c = 0.f; s = 0.f; }
+    float c;  // reference, m * k rounded (0 while m is -inf)
+    float s;  // sum of 2^(x * k - c)
+    float k;  // log2(e) / temperature
+    __device__ __forceinline__ void init(float scale) { m = neg_inf(); c = 0.f; s = 0.f; k = scale; }
     __device__ __forceinline__ void raise(float nm) {
-        const float nc = nm * kLog2e;
+        const float nc = nm * k;
         s = (s == 0.f) ? 0.f : s * ex2(c - nc);
         c = nc;
         m = nm;
     }
     // Terms of four logits: two packed FMAs, four EX2, one packed add.
     __device__ __forceinline__ float2 term4(const float4& v) const {
-        const float2 l2e = make_float2(kLog2e, kLog2e), mc = make_float2(-c, -c);
+        const float2 l2e = make_float2(k, k), mc = make_float2(-c, -c);
         const float2 y0 = ffma2(make_float2(v.x, v.y), l2e, mc);
         const float2 y1 = ffma2(make_float2(v.z, v.w), l2e, mc);
         return fadd2(make_float2(ex2(y0.x), ex2(y0.y)), make_float2(ex2(y1.x), ex2(y1.y)));
@@ -428,25 +439,27 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     }
 }
 
-// Write one finished row: K top columns and the target column.
+// Write one finished row: K top columns and the target column. (C, S) are the row's
+// reference and sum in the log2 domain of scale kk = log2(e)/tau; a logprob is
+// (x*kk - C)*ln2 - ln(S), formed in fp64.
 template <int SLOTS, bool TOPK>
 __device__ __forceinline__ void write_row(const RowsParams& p, uint32_t o, const WarpList<SLOTS>& L, float C,
-                                          float S, uint32_t t, bool has_xt, float xt, int lane) {
-    const double lse = (double)C * kLn2 + (double)logf(S);
+                                          float S, uint32_t t, bool has_xt, float xt, float kk, int lane) {
+    const double ln_s = (double)logf(S), kd = (double)kk, cd = (double)C;
     const size_t ro = (size_t)o * p.W;
     if constexpr (TOPK) {
 #pragma unroll
         for (int k = 0; k < SLOTS; ++k) {
             const uint32_t i = (uint32_t)lane + 32u * k;
             if (i < p.K) {
-                p.out_lp[ro + i] = (float)((double)L.x[k] - lse);
+                p.out_lp[ro + i] = (float)(((double)L.x[k] * kd - cd) * kLn2 - ln_s);
                 p.out_tok[ro + i] = L.id[k];
             }
         }
     }
     if (lane == 0) {
         float lpt = __int_as_float(0x7fc00000);
-        if (t < p.V && has_xt) lpt = (float)((double)xt - lse);
+        if (t < p.V && has_xt) lpt = (float)(((double)xt * kd - cd) * kLn2 - ln_s);
         if (t >= p.V) atomicOr(p.status, kStatusTokenRange);
         p.out_lp[ro + p.K] = lpt;
         p.out_tok[ro + p.K] = t;
@@ -543,11 +556,88 @@ __device__ __forceinline__ bool take_ticket(const RowsParams& p, uint64_t w0, ui
     return last;
 }
 
+// Where one output row reads and what it scores. Output row o of batch b is the
+// (o - out_off[b])-th of the batch's last cnt positions; position r scores token r+1
+// of the same sequence, the last position the batch's sampled token. Its logits row
+// counts back from the end of the batch's logits rows, which must hold cnt rows at
+// least (all positions of a sequence, or only its last ones).
+// EXT = false compiles the plain path (every position has its logits row, raw logits):
+// loff is off and k is the constant log2(e).
+struct RowDesc {
+    const float* rowp;  // logits row
+    uint32_t t;         // target token
+    float k;            // log2(e) / tau, rounded to fp32
+    uint32_t err;       // status bit, 0 if the row is valid
+};
+
+template <bool EXT>
+__device__ __forceinline__ RowDesc describe_row(const RowsParams& p, const uint32_t* off, const uint32_t* loff,
+                                                const uint32_t* out_off, const uint8_t* echo, uint32_t b,
+                                                uint32_t o) {
+    RowDesc d;
+    const uint32_t ob = out_off[b], oe = out_off[b + 1];
+    const uint32_t sb = off[b], eb = off[b + 1];
+    const uint32_t lb = EXT ? loff[b] : sb, le = EXT ? loff[b + 1] : eb;
+    const uint32_t cnt = oe - ob, len = eb - sb;
+    const bool layout_ok = (o >= ob) && (o < oe) && (eb > sb) && (eb <= p.T) && (cnt == (echo[b] ? len : 1u)) &&
+                           (!EXT || ((le >= lb) && (le - lb >= cnt) && (le <= p.T_logits)));
+    // tau must be positive and finite (NaN fails the first test) with log2(e)/tau finite
+    d.k = kLog2e;
+    bool tau_ok = true;
+    if (EXT && p.tau != nullptr) {
+        const float tau = p.tau[b];
+        d.k = __fdiv_rn(kLog2e, tau);  // fp32: its rounding is covered by the logprob form
+        tau_ok = tau > 0.f && tau <= 3.4028234663852886e38f && d.k <= 3.4028234663852886e38f;
+    }
+    d.err = !layout_ok ? kStatusOffsets : (!tau_ok ? kStatusTemperature : 0u);
+    d.t = 0;
+    d.rowp = p.logits;
+    if (d.err == 0) {
+        const uint32_t r = eb - cnt + (o - ob);
+        d.t = (r + 1 < eb) ? p.tokens[r + 1] : p.sampled[b];
+        d.rowp = p.logits + (size_t)(le - cnt + (o - ob)) * p.V;
+    }
+    return d;
+}
+
+// An invalid row gets NaN logprobs and padding ids; its status bit is raised.
+__device__ __forceinline__ void write_invalid_row(const RowsParams& p, uint32_t o, uint32_t err, int lane) {
+    for (uint32_t col = (uint32_t)lane; col < p.W; col += 32) {
+        p.out_lp[(size_t)o * p.W + col] = __int_as_float(0x7fc00000);
+        p.out_tok[(size_t)o * p.W + col] = kPadId;
+    }
+    if (lane == 0) atomicOr(p.status, err);
+}
+
+// Stage the per-batch arrays in shared memory: [off][out_off][loff if distinct][echo].
+template <bool EXT>
+__device__ __forceinline__ void stage_batch_arrays(const RowsParams& p, uint32_t* s_dyn, int tid, int nthreads,
+                                                   const uint32_t*& off, const uint32_t*& loff,
+                                                   const uint32_t*& out_off, const uint8_t*& echo) {
+    const uint32_t B = p.B;
+    const bool var = EXT && p.loff != p.off;
+    uint32_t* s_l = var ? s_dyn + 2 * (B + 1) : s_dyn;
+    uint8_t* s_e = reinterpret_cast<uint8_t*>(s_dyn + (var ? 3u : 2u) * (B + 1));
+    for (uint32_t i = (uint32_t)tid; i <= B; i += (uint32_t)nthreads) {
+        const uint32_t a0 = p.off[i], a1 = p.out_off[i];
+        const uint32_t a2 = var ? p.loff[i] : 0u;
+        const uint8_t e = i < B ? p.echo[i] : 0;
+        s_dyn[i] = a0;
+        s_dyn[B + 1 + i] = a1;
+        if (var) s_l[i] = a2;
+        if (i < B) s_e[i] = e;
+    }
+    off = s_dyn;
+    out_off = s_dyn + B + 1;
+    loff = s_l;
+    echo = s_e;
+}
+
 // Dynamic shared memory: the warps' rings, then the staged offsets.
 template <int U, int STAGES>
 __host__ __device__ constexpr uint32_t ring_bytes() { return (uint32_t)kWarps * STAGES * U * 512u; }
 
-template <int SLOTS, bool TOPK, int U, int STAGES>
+template <int SLOTS, bool TOPK, int U, int STAGES, bool EXT>
 __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) {
     extern __shared__ __align__(16) unsigned char s_raw[];
     float4* rings = reinterpret_cast<float4*>(s_raw);
@@ -562,19 +652,11 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
     const uint32_t status = __ldcg(p.status);
     const uint32_t R = __ldcg(p.out_off + B);
     const uint32_t* off = p.off;
+    const uint32_t* loff = p.loff;
     const uint32_t* out_off = p.out_off;
     const uint8_t* echo = p.echo;
     if (p.stage_offsets) {
-        for (uint32_t i = threadIdx.x; i <= B; i += kThreads) {
-            const uint32_t a0 = p.off[i], a1 = p.out_off[i];
-            const uint8_t e = i < B ? p.echo[i] : 0;
-            s_dyn[i] = a0;
-            s_dyn[B + 1 + i] = a1;
-            if (i < B) reinterpret_cast<uint8_t*>(s_dyn + 2 * (B + 1))[i] = e;
-        }
-        off = s_dyn;
-        out_off = s_dyn + B + 1;
-        echo = reinterpret_cast<const uint8_t*>(s_dyn + 2 * (B + 1));
+        stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kThreads, off, loff, out_off, echo);
         __syncthreads();
     }
     if (status & kStatusOffsets) return;  // plan rejected the offsets
@@ -609,29 +691,18 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
         const bool full = (q0 == 0) && (q1 == p.nq);
 
         // ---- row descriptor (identical in every lane) ---------------------------------
-        const uint32_t ob = out_off[b], oe = out_off[b + 1];
-        const uint32_t sb = off[b], eb = off[b + 1];
-        const uint32_t cnt = oe - ob, len = eb - sb;
-        const bool valid = (o >= ob) && (o < oe) && (eb > sb) && (eb <= p.T) &&
-                           (cnt == (echo[b] ? len : 1u));
-        if (!valid) {
-            if (q0 == 0) {
-                for (uint32_t col = (uint32_t)lane; col < p.W; col += 32) {
-                    p.out_lp[(size_t)o * p.W + col] = __int_as_float(0x7fc00000);
-                    p.out_tok[(size_t)o * p.W + col] = kPadId;
-                }
-            }
-            if (q0 == 0 && lane == 0) atomicOr(p.status, kStatusOffsets);
+        const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, b, o);
+        if (d.err) {
+            if (q0 == 0) write_invalid_row(p, o, d.err, lane);
         } else {
-            const uint32_t r = eb - cnt + (o - ob);
-            const uint32_t t = (r + 1 < eb) ? p.tokens[r + 1] : p.sampled[b];
-            const float* rowp = p.logits + (size_t)r * V;
+            const uint32_t t = d.t;
+            const float* rowp = d.rowp;
             const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
             const int64_t e_lo = 4 * (int64_t)q0 - a, e_hi = 4 * (int64_t)q1 - a;
             const bool t_here = t < V && (int64_t)t >= e_lo && (int64_t)t < e_hi;
 
             LaneSum ls;
-            ls.init();
+            ls.init(d.k);
             Selector<SLOTS> sel;
             sel.init(s_cx[w], s_ci[w], K);
             float xt = 0.f;
@@ -658,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
                     if (lane == 0) p.counters[w0] = 0u;  // ready for the next call
                 }
             }
-            if (emit) write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, has_xt, xt_row, lane);
+            if (emit) write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, has_xt, xt_row, d.k, lane);
         }
 
         // ---- next piece -----------------------------------------------------------
@@ -693,7 +764,7 @@ constexpr int kQueueWarps = LP_QUEUE_WARPS;
 constexpr int kQueueStages = LP_QUEUE_STAGES;
 constexpr int kQueueUnroll = LP_QUEUE_UNROLL;
 
-template <int SLOTS, bool TOPK, int U, int STAGES, int NW>
+template <int SLOTS, bool TOPK, int U, int STAGES, int NW, bool EXT>
 __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     extern __shared__ __align__(16) unsigned char s_raw[];
     float4* rings = reinterpret_cast<float4*>(s_raw);
@@ -709,20 +780,10 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const uint32_t status = __ldcg(p.status);
     const uint32_t R = __ldcg(p.out_off + B);
     const uint32_t* off = p.off;
+    const uint32_t* loff = p.loff;
     const uint32_t* out_off = p.out_off;
     const uint8_t* echo = p.echo;
-    if (p.stage_offsets) {
-        for (uint32_t i = threadIdx.x; i <= B; i += kT) {
-            const uint32_t a0 = p.off[i], a1 = p.out_off[i];
-            const uint8_t e = i < B ? p.echo[i] : 0;
-            s_dyn[i] = a0;
-            s_dyn[B + 1 + i] = a1;
-            if (i < B) reinterpret_cast<uint8_t*>(s_dyn + 2 * (B + 1))[i] = e;
-        }
-        off = s_dyn;
-        out_off = s_dyn + B + 1;
-        echo = reinterpret_cast<const uint8_t*>(s_dyn + 2 * (B + 1));
-    }
+    if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo);
     if (threadIdx.x == 0) { cm.has_xt = 0u; cm.thr = 0u; }
     uint32_t* queue = p.counters;  // [0] next row, [1] CTAs finished, [2 + sm] CTAs of that SM
     bool bad = (status & kStatusOffsets) || R > p.T;
@@ -750,26 +811,14 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             const uint32_t mid = (lo + hi) >> 1;
             if (out_off[mid] <= o) lo = mid; else hi = mid;
         }
-        const uint32_t b = lo;
-        const uint32_t ob = out_off[b], oe = out_off[b + 1];
-        const uint32_t sb = off[b], eb = off[b + 1];
-        const uint32_t cnt = oe - ob, len = eb - sb;
-        const bool valid = (o >= ob) && (o < oe) && (eb > sb) && (eb <= p.T) &&
-                           (cnt == (echo[b] ? len : 1u));
-        if (!valid) {
-            if (w == 0) {
-                for (uint32_t col = (uint32_t)lane; col < p.W; col += 32) {
-                    p.out_lp[(size_t)o * p.W + col] = __int_as_float(0x7fc00000);
-                    p.out_tok[(size_t)o * p.W + col] = kPadId;
-                }
-                if (lane == 0) atomicOr(p.status, kStatusOffsets);
-            }
+        const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, lo, o);
+        if (d.err) {
+            if (w == 0) write_invalid_row(p, o, d.err, lane);
             __syncthreads();
             continue;
         }
-        const uint32_t r = eb - cnt + (o - ob);
-        const uint32_t t = (r + 1 < eb) ? p.tokens[r + 1] : p.sampled[b];
-        const float* rowp = p.logits + (size_t)r * V;
+        const uint32_t t = d.t;
+        const float* rowp = d.rowp;
         const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
         const uint32_t wq0 = (uint32_t)(((uint64_t)p.nq * w) / NW);
         const uint32_t wq1 = (uint32_t)(((uint64_t)p.nq * (w + 1)) / NW);
@@ -777,7 +826,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         const bool t_here = t < V && (int64_t)t >= e_lo && (int64_t)t < e_hi;
 
         LaneSum ls;
-        ls.init();
+        ls.init(d.k);
         Selector<SLOTS> sel;
         sel.init(s_cx[w], s_ci[w], K);
         float xt = 0.f;
@@ -824,7 +873,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             S = 0.f;
             for (int j = lane; j < NW; j += 32) lse2_combine(C, S, cm.red_c[j], cm.red_s[j]);
             warp_lse2_reduce(C, S);
-            write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, lane);
+            write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, d.k, lane);
             __syncwarp();
             if (lane == 0) { cm.has_xt = 0u; cm.thr = 0u; }
         }

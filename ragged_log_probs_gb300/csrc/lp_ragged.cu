@@ -22,20 +22,22 @@ constexpr uint32_t kStageOffsetsMax = 2048;     // stage off/out_off in smem whe
 constexpr uint32_t kUnroll = LP_UNROLL;
 constexpr uint32_t kStages = LP_STAGES;
 constexpr size_t kRingBytes = lpk::ring_bytes<kUnroll, kStages>();
-// Largest dynamic shared memory a launch asks for: the rings + staged offsets/echo.
-constexpr size_t kMaxDynSmem = kRingBytes + 2 * kStageOffsetsMax * 4 + kStageOffsetsMax;
+// Largest dynamic shared memory a launch asks for: the rings + staged offsets (input
+// positions, output rows, logits rows when they differ) and echo flags.
+constexpr size_t kMaxDynSmem = kRingBytes + 3 * kStageOffsetsMax * 4 + kStageOffsetsMax;
 constexpr int kQW = lpk::kQueueWarps;  // warps per CTA of the row-queue kernel
 constexpr int kQS = lpk::kQueueStages;
 constexpr int kQU = lpk::kQueueUnroll;
 constexpr size_t kQueueRingBytes = (size_t)kQW * kQS * kQU * 512;
-constexpr size_t kMaxDynSmemQueue = kQueueRingBytes + 2 * kStageOffsetsMax * 4 + kStageOffsetsMax;
+constexpr size_t kMaxDynSmemQueue = kQueueRingBytes + 3 * kStageOffsetsMax * 4 + kStageOffsetsMax;
 // Dynamic shared memory the row-queue kernel may ask for next to its ~17 KB of static
 // shared memory (227 KB per CTA in all).
 constexpr size_t kQueueDynSmemBudget = 208 * 1024;
 #ifndef LP_PDL
 #define LP_PDL 1  // launch the row kernel as a programmatic dependent of the plan
 #endif
-constexpr int kVariants = 6;                    // (levels 0 | 1..5 | 6) x (warp ranges | row queue)
+// (levels 0 | 1..5 | 6) x (warp ranges | row queue) x (plain | extended inputs)
+constexpr int kVariants = 12;
 
 struct DeviceInfo {
     bool ready = false;
@@ -48,16 +50,24 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
-const void* variant_fn(int v) {
+using RowsKernel = void (*)(lpk::RowsParams);
+
+template <bool EXT>
+RowsKernel variant_kernel(int v) {
     switch (v) {
-        case 0: return reinterpret_cast<const void*>(&lpk::k_rows<1, false, kUnroll, kStages>);
-        case 1: return reinterpret_cast<const void*>(&lpk::k_rows<1, true, kUnroll, kStages>);
-        case 2: return reinterpret_cast<const void*>(&lpk::k_rows<2, true, kUnroll, kStages>);
-        case 3: return reinterpret_cast<const void*>(&lpk::k_rows_cta<1, false, kQU, kQS, kQW>);
-        case 4: return reinterpret_cast<const void*>(&lpk::k_rows_cta<1, true, kQU, kQS, kQW>);
-        default: return reinterpret_cast<const void*>(&lpk::k_rows_cta<2, true, kQU, kQS, kQW>);
+        case 0: return &lpk::k_rows<1, false, kUnroll, kStages, EXT>;
+        case 1: return &lpk::k_rows<1, true, kUnroll, kStages, EXT>;
+        case 2: return &lpk::k_rows<2, true, kUnroll, kStages, EXT>;
+        case 3: return &lpk::k_rows_cta<1, false, kQU, kQS, kQW, EXT>;
+        case 4: return &lpk::k_rows_cta<1, true, kQU, kQS, kQW, EXT>;
+        default: return &lpk::k_rows_cta<2, true, kQU, kQS, kQW, EXT>;
     }
 }
+
+// Variant v: (v % 6) picks levels class and kernel (>= 3: row queue); v >= 6 extended inputs.
+RowsKernel variant_kernel(int v) { return v >= 6 ? variant_kernel<true>(v - 6) : variant_kernel<false>(v); }
+bool is_queue(int v) { return (v % 6) >= 3; }
+const void* variant_fn(int v) { return reinterpret_cast<const void*>(variant_kernel(v)); }
 
 int variant_of(uint32_t levels) { return levels == 0 ? 0 : (levels < 6 ? 1 : 2); }
 
@@ -82,7 +92,7 @@ int occupancy(DeviceInfo* d, int v, size_t smem) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!d->smem_attr[v]) {
         if (cudaFuncSetAttribute(variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(v >= 3 ? kMaxDynSmemQueue : kMaxDynSmem)) != cudaSuccess) {
+                                 (int)(is_queue(v) ? kMaxDynSmemQueue : kMaxDynSmem)) != cudaSuccess) {
             (void)cudaGetLastError();
             return 0;
         }
@@ -90,7 +100,7 @@ int occupancy(DeviceInfo* d, int v, size_t smem) {
     }
     if (d->occ[v] == 0 || d->occ_smem[v] != smem) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, variant_fn(v), v >= 3 ? kQW * 32 : lpk::kThreads,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, variant_fn(v), is_queue(v) ? kQW * 32 : lpk::kThreads,
                                                           smem) != cudaSuccess)
             n = 1;
         if (n < 1) n = 1;
@@ -153,17 +163,19 @@ lp_status lp_ragged_plan(const uint32_t* logit_row_offsets, const uint8_t* echo,
     return LP_OK;
 }
 
-lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const uint32_t* logit_row_offsets,
-                            uint32_t B, const uint32_t* tokens, const uint32_t* sampled_tokens,
-                            const uint32_t* output_row_offsets, const uint8_t* echo, uint32_t levels,
-                            float* out_logprobs, uint32_t* out_tokens, void* workspace, size_t workspace_bytes,
-                            lp_stream_t stream) {
+lp_status lp_ragged_compute_ex(const float* logits, uint32_t T_logits, uint32_t V,
+                               const uint32_t* logit_row_offsets, const uint32_t* input_row_offsets, uint32_t T,
+                               uint32_t B, const uint32_t* tokens, const uint32_t* sampled_tokens,
+                               const uint32_t* output_row_offsets, const uint8_t* echo, const float* temperatures,
+                               uint32_t levels, float* out_logprobs, uint32_t* out_tokens, void* workspace,
+                               size_t workspace_bytes, lp_stream_t stream) {
     if (!logits || !logit_row_offsets || !tokens || !sampled_tokens || !output_row_offsets || !echo ||
         !out_logprobs || !out_tokens)
         return LP_ERR_NULL;
     if (!workspace) return LP_ERR_WORKSPACE;
     if (levels > LP_MAX_LEVELS) return LP_ERR_LEVELS;
-    if (B == 0 || T == 0 || V == 0 || V >= 0x7FFFFFFFu) return LP_ERR_SHAPE;
+    if (!input_row_offsets && T != T_logits) return LP_ERR_SHAPE;
+    if (B == 0 || T == 0 || T_logits == 0 || V == 0 || V >= 0x7FFFFFFFu) return LP_ERR_SHAPE;
     if (((uintptr_t)logits & 3u) != 0) return LP_ERR_SHAPE;
     if (((uintptr_t)workspace & 255u) != 0) return LP_ERR_WORKSPACE;
     int dev;
@@ -178,7 +190,9 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
 
     lpk::RowsParams p;
     p.logits = logits;
-    p.off = logit_row_offsets;
+    p.off = input_row_offsets ? input_row_offsets : logit_row_offsets;
+    p.loff = logit_row_offsets;
+    p.tau = temperatures;
     p.tokens = tokens;
     p.sampled = sampled_tokens;
     p.out_off = output_row_offsets;
@@ -189,6 +203,7 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
     p.counters = reinterpret_cast<uint32_t*>(ws + sizeof(lpk::WsHeader));
     p.partials = ws + sizeof(lpk::WsHeader) + counters_bytes(g_max);
     p.T = T;
+    p.T_logits = T_logits;
     p.V = V;
     p.B = B;
     p.K = K;
@@ -200,16 +215,22 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
     p.stage_offsets = (B + 1u <= kStageOffsetsMax) ? 1u : 0u;
     p.num_sms = (uint32_t)d->sms;
 
-    const size_t smem = kRingBytes + (p.stage_offsets ? (size_t)2 * (B + 1u) * sizeof(uint32_t) + ((B + 3u) & ~3u) : 0);
+    const uint32_t staged_arrays = (p.loff != p.off) ? 3u : 2u;
+    const size_t smem =
+        kRingBytes + (p.stage_offsets ? (size_t)staged_arrays * (B + 1u) * sizeof(uint32_t) + ((B + 3u) & ~3u) : 0);
 
-    // Row queue when even all-echo input (R <= T) gives fewer rows than half the warps;
-    // otherwise warp-owned ranges of the row space (the two kernels give the same result).
-    int v = variant_of(levels);
+    // Row queue when even all-echo input (R <= T, and R <= T_logits) gives fewer rows than
+    // half the warps; otherwise warp-owned ranges of the row space (the two kernels give
+    // the same result).
+    // Plain instantiation unless an extended input is given (it compiles without them).
+    const bool ext = input_row_offsets != nullptr || temperatures != nullptr;
+    int v = variant_of(levels) + (ext ? 6 : 0);
     int occ = occupancy(d, v, smem);
     if (occ == 0) return LP_ERR_CUDA;
     uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;  // occ <= kMaxCtasPerSm
     const char* force = std::getenv("LP_RAGGED_KERNEL");  // test hook: "warp" or "queue"
-    bool queue = 2ull * T < (uint64_t)grid * lpk::kWarps;
+    const uint32_t r_max = T < T_logits ? T : T_logits;
+    bool queue = 2ull * r_max < (uint64_t)grid * lpk::kWarps;
     if (force && std::strcmp(force, "warp") == 0) queue = false;
     if (force && std::strcmp(force, "queue") == 0) queue = true;
     size_t launch_smem = smem;
@@ -231,23 +252,25 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(v >= 3 ? kQW * 32 : lpk::kThreads);
+    cfg.blockDim = dim3(queue ? kQW * 32 : lpk::kThreads);
     cfg.dynamicSmemBytes = launch_smem;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cfg.attrs = attr;
     cfg.numAttrs = LP_PDL ? 1 : 0;
-    cudaError_t err;
-    switch (v) {
-        case 0: err = cudaLaunchKernelEx(&cfg, lpk::k_rows<1, false, kUnroll, kStages>, p); break;
-        case 1: err = cudaLaunchKernelEx(&cfg, lpk::k_rows<1, true, kUnroll, kStages>, p); break;
-        case 2: err = cudaLaunchKernelEx(&cfg, lpk::k_rows<2, true, kUnroll, kStages>, p); break;
-        case 3: err = cudaLaunchKernelEx(&cfg, lpk::k_rows_cta<1, false, kQU, kQS, kQW>, p); break;
-        case 4: err = cudaLaunchKernelEx(&cfg, lpk::k_rows_cta<1, true, kQU, kQS, kQW>, p); break;
-        default: err = cudaLaunchKernelEx(&cfg, lpk::k_rows_cta<2, true, kQU, kQS, kQW>, p); break;
-    }
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, variant_kernel(v), p);
     if (err != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
     if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
     return LP_OK;
+}
+
+lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const uint32_t* logit_row_offsets,
+                            uint32_t B, const uint32_t* tokens, const uint32_t* sampled_tokens,
+                            const uint32_t* output_row_offsets, const uint8_t* echo, uint32_t levels,
+                            float* out_logprobs, uint32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                            lp_stream_t stream) {
+    return lp_ragged_compute_ex(logits, T, V, logit_row_offsets, nullptr, T, B, tokens, sampled_tokens,
+                                output_row_offsets, echo, nullptr, levels, out_logprobs, out_tokens, workspace,
+                                workspace_bytes, stream);
 }
 
 lp_status lp_ragged_read_status(const void* workspace, uint32_t* host_status, lp_stream_t stream) {
@@ -265,10 +288,13 @@ const char* lp_ragged_strerror(lp_status status) {
         case LP_ERR_NULL: return "a required pointer is NULL";
         case LP_ERR_LEVELS: return "levels exceeds 6 (top-k capacity 63)";
         case LP_ERR_SHAPE: return "B, T or V is zero or too large, or logits are not 4-byte aligned";
-        case LP_ERR_OFFSETS: return "row offsets invalid: empty/decreasing batch, range past T, or echo mismatch";
+        case LP_ERR_OFFSETS:
+            return "row offsets invalid: empty/decreasing batch, range past T, echo mismatch, or fewer logits "
+                   "rows than scored positions";
         case LP_ERR_TOKEN_RANGE: return "an actual or sampled token id is >= V";
         case LP_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case LP_ERR_CUDA: return "CUDA launch or copy failed";
+        case LP_ERR_TEMPERATURE: return "a temperature is not a positive finite number";
         default: return "unknown lp_status";
     }
 }

@@ -25,7 +25,8 @@ def run_gpu(batch, workspace=None):
     import ragged_log_probs_gb300 as lp
     out_off, out_lp, out_tok = lp.ragged_log_probs(batch.logits, batch.logit_row_offsets, batch.tokens,
                                                    batch.sampled_tokens, batch.echo, batch.levels,
-                                                   workspace=workspace)
+                                                   workspace=workspace, input_row_offsets=batch.input_row_offsets,
+                                                   temperatures=batch.temperatures)
     torch.cuda.synchronize()
     return (out_off.cpu().numpy().view(np.uint32).astype(np.uint64), out_lp.cpu().numpy(),
             out_tok.cpu().numpy().view(np.uint32).astype(np.uint64))
@@ -44,10 +45,13 @@ def row_getter(logits: torch.Tensor):
 
 def oracle_for(batch, rows=None, full_copy=None):
     off, tokens, sampled, echo = batch.host()
+    ioff, tau = batch.host_variant()
     if full_copy is None:
         full_copy = batch.logits.numel() * 4 <= (1 << 31)
     src = batch.logits.cpu().numpy() if full_copy else row_getter(batch.logits)
-    return oracle.ragged_log_probs(src, off, tokens, sampled, echo, batch.levels, rows=rows, T=batch.T)
+    return oracle.ragged_log_probs(src, off, tokens, sampled, echo, batch.levels, rows=rows, T=batch.T,
+                                   temperatures=None if tau is None else [float(t) for t in tau],
+                                   input_row_offsets=ioff)
 
 
 def compare(gpu_lp, gpu_tok, ref_lp, ref_tok, what=""):

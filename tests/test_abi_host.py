@@ -12,6 +12,7 @@ HEADER = os.path.join(ROOT, "include", "lp_ragged.h")
 
 LP_OK, LP_ERR_NULL, LP_ERR_LEVELS, LP_ERR_SHAPE = 0, 1, 2, 3
 LP_ERR_OFFSETS, LP_ERR_TOKEN_RANGE, LP_ERR_WORKSPACE, LP_ERR_CUDA = 4, 5, 6, 7
+LP_ERR_TEMPERATURE = 8
 FAKE = 0x10000          # non-NULL, 256-byte aligned, never dereferenced: each call returns first
 
 
@@ -30,7 +31,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert set(declared_functions()) >= {"lp_ragged_workspace_size", "lp_ragged_plan", "lp_ragged_compute",
-                                         "lp_ragged_read_status", "lp_ragged_strerror"}
+                                         "lp_ragged_compute_ex", "lp_ragged_read_status", "lp_ragged_strerror"}
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -40,11 +41,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_strerror_covers_codes(lib):
     seen = set()
-    for code in range(8):
+    for code in range(LP_ERR_TEMPERATURE + 1):
         s = lib.lp_ragged_strerror(code).decode()
         assert s and s != "unknown lp_status"
         seen.add(s)
-    assert len(seen) == 8
+    assert len(seen) == LP_ERR_TEMPERATURE + 1
     assert lib.lp_ragged_strerror(99).decode() == "unknown lp_status"
 
 
@@ -66,6 +67,26 @@ def test_compute_host_checks(lib):
     assert _compute(lib, V=0x7FFFFFFF) == LP_ERR_SHAPE
     assert _compute(lib, logits=FAKE + 2) == LP_ERR_SHAPE
     assert _compute(lib, ws=FAKE + 16) == LP_ERR_WORKSPACE
+
+
+def _compute_ex(lib, logits=FAKE, T_logits=4, V=100, loff=FAKE, ioff=None, T=4, B=2, tokens=FAKE, sampled=FAKE,
+                out_off=FAKE, echo=FAKE, tau=None, levels=3, out_lp=FAKE, out_tok=FAKE, ws=FAKE, ws_bytes=1 << 20):
+    return lib.lp_ragged_compute_ex(logits, T_logits, V, loff, ioff, T, B, tokens, sampled, out_off, echo, tau,
+                                    levels, out_lp, out_tok, ws, ws_bytes, None)
+
+
+def test_compute_ex_host_checks(lib):
+    assert _compute_ex(lib, logits=None) == LP_ERR_NULL
+    assert _compute_ex(lib, loff=None) == LP_ERR_NULL
+    assert _compute_ex(lib, sampled=None) == LP_ERR_NULL
+    assert _compute_ex(lib, ws=None) == LP_ERR_WORKSPACE
+    assert _compute_ex(lib, levels=7) == LP_ERR_LEVELS
+    assert _compute_ex(lib, T=6) == LP_ERR_SHAPE              # no input offsets: T must equal T_logits
+    assert _compute_ex(lib, ioff=FAKE, T_logits=0) == LP_ERR_SHAPE
+    assert _compute_ex(lib, ioff=FAKE, T=0) == LP_ERR_SHAPE
+    assert _compute_ex(lib, V=0) == LP_ERR_SHAPE
+    assert _compute_ex(lib, logits=FAKE + 1) == LP_ERR_SHAPE
+    assert _compute_ex(lib, ws=FAKE + 64) == LP_ERR_WORKSPACE
 
 
 def test_plan_host_checks(lib):

@@ -19,6 +19,12 @@ dataset, so nothing real is replaced):
 * ``wide``    B=32, lengths U[128, 1024], V=256000, levels=6, all echo; N(0, 1)
               rounded to multiples of 1/16 (many exact ties).
 
+Two input variants apply to any workload: per-batch temperatures
+(``with_temperatures``: uniform in [0.25, 2.0], some exactly 1.0) and VARIABLE
+logits (``make_batch(..., variable_extra=n)``: the logits tensor holds only each
+sequence's last positions — all of them for echo batches, 1 + U{0..n} (capped by the
+length) otherwise — and ``input_row_offsets`` describes the positions).
+
 Host-side structure comes from ``numpy.random.default_rng(seed)``; logits come from
 a ``torch.Generator`` on the target device, drawn in fixed row chunks so the values
 depend only on (seed, shape, device type).
@@ -52,15 +58,17 @@ _CHUNK_ROWS = 512
 class Batch:
     """One ragged batch. Integer tensors are int32 storage of uint32 values."""
     name: str
-    logits: torch.Tensor            # f32 [T, V]
-    logit_row_offsets: torch.Tensor  # int32 [B+1]
-    tokens: torch.Tensor            # int32 [T]
+    logits: torch.Tensor            # f32 [T, V] (VARIABLE: [T_logits, V])
+    logit_row_offsets: torch.Tensor  # int32 [B+1], rows of ``logits`` per batch
+    tokens: torch.Tensor            # int32 [T_in]
     sampled_tokens: torch.Tensor    # int32 [B]
     echo: torch.Tensor              # uint8 [B]
     levels: int
     B: int
-    T: int
+    T: int                          # rows of ``logits``
     V: int
+    input_row_offsets: Optional[torch.Tensor] = None  # int32 [B+1], positions (VARIABLE only)
+    temperatures: Optional[torch.Tensor] = None       # f32 [B]
 
     def host(self):
         """numpy copies of the integer inputs (logits stay where they are)."""
@@ -68,6 +76,16 @@ class Batch:
                 self.tokens.cpu().numpy().view(np.uint32),
                 self.sampled_tokens.cpu().numpy().view(np.uint32),
                 self.echo.cpu().numpy().astype(bool))
+
+    def host_variant(self):
+        """numpy copies of the optional inputs: (input offsets or None, temperatures or None)."""
+        ioff = None if self.input_row_offsets is None else self.input_row_offsets.cpu().numpy().view(np.uint32)
+        tau = None if self.temperatures is None else self.temperatures.cpu().numpy().astype(np.float32)
+        return ioff, tau
+
+    @property
+    def positions_offsets(self) -> torch.Tensor:
+        return self.logit_row_offsets if self.input_row_offsets is None else self.input_row_offsets
 
 
 def _fill_logits(out: torch.Tensor, dist: str, scale: float, gen: torch.Generator,
@@ -114,9 +132,11 @@ def _duplicate_max(logits: torch.Tensor, rows, rng: np.random.Generator) -> None
 
 def make_batch(name: str, device="cpu", *, B: Optional[int] = None, V: Optional[int] = None,
                max_len: Optional[int] = None, levels: Optional[int] = None,
-               seed: Optional[int] = None) -> Batch:
+               seed: Optional[int] = None, variable_extra: Optional[int] = None) -> Batch:
     """Build a named workload, optionally shrunk (fewer batches, smaller vocab,
-    shorter sequences) while keeping its distribution and structure."""
+    shorter sequences) while keeping its distribution and structure.
+
+    ``variable_extra`` switches to VARIABLE logits (see the module docstring)."""
     cfg = dict(CONFIGS[name])
     seed = cfg["seed"] if seed is None else seed
     rng = np.random.default_rng(seed)
@@ -153,6 +173,15 @@ def make_batch(name: str, device="cpu", *, B: Optional[int] = None, V: Optional[
     T = int(offsets[-1])
     tokens = rng.integers(0, Vn, size=T, dtype=np.int64)
     sampled = rng.integers(0, Vn, size=Bn, dtype=np.int64)
+    input_offsets = None
+    if variable_extra is not None:
+        # present logits rows: all positions of an echo batch, else the last 1 + extra
+        extra = rng.integers(0, variable_extra + 1, size=Bn)
+        present = np.where(echo != 0, lengths, np.minimum(lengths, 1 + extra))
+        input_offsets = offsets
+        offsets = np.zeros(Bn + 1, dtype=np.int64)
+        offsets[1:] = np.cumsum(present)
+        T = int(offsets[-1])
 
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
@@ -170,9 +199,23 @@ def make_batch(name: str, device="cpu", *, B: Optional[int] = None, V: Optional[
     _duplicate_max(logits, [r for r in tie_rows if r < T], rng)
 
     as_i32 = lambda a: torch.from_numpy(np.asarray(a, dtype=np.int64).astype(np.uint32).view(np.int32)).to(dev)
-    return Batch(name=name, logits=logits, logit_row_offsets=as_i32(offsets), tokens=as_i32(tokens),
+    return Batch(name=name if variable_extra is None else name + "_variable", logits=logits,
+                 logit_row_offsets=as_i32(offsets), tokens=as_i32(tokens),
                  sampled_tokens=as_i32(sampled), echo=torch.from_numpy(echo).to(dev),
-                 levels=lv, B=Bn, T=T, V=Vn)
+                 levels=lv, B=Bn, T=T, V=Vn,
+                 input_row_offsets=None if input_offsets is None else as_i32(input_offsets))
+
+
+def with_temperatures(batch: Batch, seed: int = 0, lo: float = 0.25, hi: float = 2.0,
+                      values=None) -> Batch:
+    """The same batch with per-batch temperatures: uniform in [lo, hi] with every
+    fourth batch exactly 1.0, or the given ``values``."""
+    if values is None:
+        rng = np.random.default_rng(seed + 7919)
+        values = rng.uniform(lo, hi, size=batch.B)
+        values[::4] = 1.0
+    tau = torch.tensor(np.asarray(values, dtype=np.float32), device=batch.logits.device)
+    return dataclasses.replace(batch, name=batch.name + "_tau", temperatures=tau)
 
 
 def make_next_token_batch(B: int, V: int, levels: int, dist: str = "normal", scale: float = 1.0,
