@@ -8,6 +8,7 @@ from .ragged_oracle import (  # noqa: F401
     PAD_ID,
     assemble,
     levels_for_top_n,
+    merge_shard_partials,
     out_per_token,
     output_row_offsets,
     output_rows,
@@ -15,6 +16,7 @@ from .ragged_oracle import (  # noqa: F401
     row_logsumexp,
     row_top_k_ids,
     score_row,
+    shard_partial,
     top_k_capacity,
     validate_offsets,
 )

@@ -36,6 +36,12 @@ Readings taken where the pages are silent (each is also listed in the design doc):
   logprob": the logprobs reuse the softmax taken after temperature scaling) the
   values are ``x_v / tau_b - logsumexp(x / tau_b)``; the top-k ranking stays on the
   raw fp32 logits, which is the same order because ``tau_b > 0``.
+* Vocab-parallel form (the SGLang page runs the forward pass on "TP worker"s; with the
+  lm_head split by vocabulary each rank holds a contiguous column range): a shard
+  summarises a row as (logsumexp of its columns, its top-k with global ids, the target
+  logit if it holds the target); merging the shards' summaries gives exactly the
+  unsharded row, because logsumexp and "k best under (logit desc, id asc)" both
+  decompose over a partition of the columns.
 * VARIABLE logits (MAX page, "echo 的前置条件：ReturnLogits 枚举"): when the input
   positions are given separately, batch ``b``'s logits rows
   ``[loff[b], loff[b+1])`` hold its LAST ``loff[b+1] - loff[b]`` positions, which
@@ -202,6 +208,51 @@ def score_row(x32: np.ndarray, target: int, levels: int,
     in_range = 0 <= target < V
     tok[K] = target
     lp[K] = (x[target] - lse) if in_range else math.nan
+    return lp, tok, in_range
+
+
+def shard_partial(x32_shard: np.ndarray, vocab_base: int, target: int, k: int, temperature: float = 1.0):
+    """Summary of one row over the columns ``[vocab_base, vocab_base + V_s)`` it holds.
+
+    Returns ``(lse_s, top, xt)``: the fp64 logsumexp of ``x / temperature`` over the
+    shard, the shard's ``k`` best ``(fp32 logit, global id)`` pairs under (logit desc,
+    id asc) without padding, and the target's fp32 logit or None when the target is
+    not in the shard."""
+    x = np.asarray(x32_shard, dtype=np.float32)
+    lse_s = row_logsumexp(x, temperature)
+    ids = row_top_k_ids(x, min(k, x.shape[0]))
+    top = [(float(x[int(i)]), vocab_base + int(i)) for i in ids if int(i) != PAD_ID]
+    local = target - vocab_base
+    xt = float(x[local]) if 0 <= local < x.shape[0] else None
+    return lse_s, top, xt
+
+
+def merge_shard_partials(partials, target: int, vocab_size: int, levels: int, temperature: float = 1.0):
+    """One output row from the shards' summaries (same layout as ``score_row``).
+
+    lse = log(sum_s exp(lse_s)) (fp64, max-shifted); the top-k is the k best of the
+    union of the shards' lists under (logit desc, global id asc); the target column
+    takes the holder's logit."""
+    K = top_k_capacity(levels)
+    W = out_per_token(levels)
+    lses = np.asarray([p[0] for p in partials], dtype=np.float64)
+    m = lses.max()
+    lse = float(m + np.log(np.sum(np.exp(lses - m))))
+    pool = [pair for p in partials for pair in p[1]]
+    pool.sort(key=lambda xi: (-xi[0], xi[1]))
+    lp = np.empty(W, dtype=np.float64)
+    tok = np.empty(W, dtype=np.uint64)
+    for c in range(K):
+        if c < len(pool):
+            tok[c] = pool[c][1]
+            lp[c] = np.float64(pool[c][0]) / np.float64(temperature) - lse
+        else:
+            tok[c] = PAD_ID
+            lp[c] = -math.inf
+    holders = [p[2] for p in partials if p[2] is not None]
+    in_range = 0 <= target < vocab_size and len(holders) == 1
+    tok[K] = target
+    lp[K] = (np.float64(holders[0]) / np.float64(temperature) - lse) if in_range else math.nan
     return lp, tok, in_range
 
 

@@ -108,12 +108,39 @@ def _rows_variable_reads_first_present(logit_row_offsets, echo, tokens, sampled,
     return out
 
 
+def _shard_partial_local_ids(x32_shard, vocab_base, target, k, temperature=1.0):
+    return _orig_shard_partial(x32_shard, 0, target - vocab_base, k, temperature)
+
+
+def _merge_ties_by_shard_last(partials, target, vocab_size, levels, temperature=1.0):
+    # pools the later shards first and sorts by logit only: ties go to the later shard
+    K = ro.top_k_capacity(levels)
+    W = ro.out_per_token(levels)
+    lses = np.asarray([p[0] for p in partials], dtype=np.float64)
+    m = lses.max()
+    lse = float(m + np.log(np.sum(np.exp(lses - m))))
+    pool = [pair for p in reversed(partials) for pair in p[1]]
+    pool.sort(key=lambda xi: -xi[0])
+    lp = np.full(W, -math.inf)
+    tok = np.full(W, oracle.PAD_ID, dtype=np.uint64)
+    for c in range(min(K, len(pool))):
+        tok[c] = pool[c][1]
+        lp[c] = pool[c][0] / temperature - lse
+    holders = [p[2] for p in partials if p[2] is not None]
+    ok = 0 <= target < vocab_size and len(holders) == 1
+    tok[K] = target
+    lp[K] = holders[0] / temperature - lse if ok else math.nan
+    return lp, tok, ok
+
+
 def _out_per_token_no_slot(levels):
     return 2 ** levels - 1 if levels > 0 else 1
 
 
 _orig_score_row = ro.score_row
 _orig_output_rows = ro.output_rows
+_orig_shard_partial = ro.shard_partial
+_orig_merge = ro.merge_shard_partials
 
 MUTATIONS = {
     "lse_drops_log": ("row_logsumexp", _lse_without_log),
@@ -128,6 +155,8 @@ MUTATIONS = {
     "temperature_multiplies": ("score_row", _score_row_multiplies_temperature),
     "temperature_lse_unscaled": ("score_row", _score_row_lse_unscaled),
     "variable_reads_first_present_rows": ("output_rows", _rows_variable_reads_first_present),
+    "shard_ids_not_offset": ("shard_partial", _shard_partial_local_ids),
+    "shard_merge_ties_by_later_shard": ("merge_shard_partials", _merge_ties_by_shard_last),
 }
 
 

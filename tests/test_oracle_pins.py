@@ -373,3 +373,56 @@ def test_variable_too_few_rows_rejected():
     with pytest.raises(ValueError):   # echo batch of 3 positions with 2 logits rows
         oracle.ragged_log_probs(x, [0, 2, 4], list(range(5)), [0, 0], [True, False], 1,
                                 input_row_offsets=[0, 3, 5])
+
+
+# --- vocab-parallel form (lm_head split by vocabulary across tensor-parallel ranks) -------
+
+def _split(V, cuts):
+    edges = [0] + sorted(cuts) + [V]
+    return [(a, b) for a, b in zip(edges[:-1], edges[1:]) if b > a]
+
+
+def test_shard_merge_hand_example():
+    # Row [1, 3, 2 | 3, 0, 2] split after column 3, K = 3, target id 4. Worked by hand:
+    # the two 3's tie across the boundary (id 1 before id 3), then the two 2's (id 2
+    # before id 5): top = ids 1, 3, 2; the target's logit 0 lives in shard 1.
+    x = np.array([1, 3, 2, 3, 0, 2], dtype=np.float32)
+    parts = [oracle.shard_partial(x[0:3], 0, 4, 3), oracle.shard_partial(x[3:6], 3, 4, 3)]
+    assert parts[0][1] == [(3.0, 1), (2.0, 2), (1.0, 0)] and parts[0][2] is None
+    assert parts[1][1] == [(3.0, 3), (2.0, 5), (0.0, 4)] and parts[1][2] == 0.0
+    lp, tok, ok = oracle.merge_shard_partials(parts, 4, 6, 2)
+    assert ok and tok.tolist() == [1, 3, 2, 4]
+    z = math.log(math.fsum(math.exp(v) for v in (1, 3, 2, 3, 0, 2)))
+    np.testing.assert_allclose(lp, [3 - z, 3 - z, 2 - z, 0 - z], atol=1e-14, rtol=0)
+
+
+def test_shard_merge_equals_unsharded_row():
+    rng = np.random.default_rng(31)
+    for trial in range(60):
+        V = int(rng.integers(1, 300))
+        x = (np.round(rng.standard_normal(V) * 3) / 2).astype(np.float32)   # many ties
+        if trial % 7 == 0:
+            x[rng.integers(0, V, size=max(1, V // 5))] = -np.inf
+        if np.all(np.isneginf(x)):
+            x[0] = 1.0
+        n_cuts = int(rng.integers(0, min(8, V)))
+        shards = _split(V, rng.choice(np.arange(1, V), size=n_cuts, replace=False).tolist() if n_cuts else [])
+        levels = int(rng.integers(0, 7))
+        K = oracle.top_k_capacity(levels)
+        t = int(rng.integers(0, V))
+        tau = [1.0, 0.6, 1.9][trial % 3]
+        parts = [oracle.shard_partial(x[a:b], a, t, K, tau) for a, b in shards]
+        lp, tok, ok = oracle.merge_shard_partials(parts, t, V, levels, tau)
+        ref_lp, ref_tok, ref_ok = oracle.score_row(x, t, levels, tau)
+        assert ok == ref_ok
+        assert tok.tolist() == ref_tok.tolist(), (trial, shards)
+        fin = np.isfinite(ref_lp)
+        assert np.array_equal(np.isneginf(lp), np.isneginf(ref_lp))
+        np.testing.assert_allclose(lp[fin], ref_lp[fin], atol=1e-11, rtol=0)
+
+
+def test_shard_target_outside_every_shard_is_nan():
+    x = np.zeros(8, dtype=np.float32)
+    parts = [oracle.shard_partial(x[0:4], 0, 8, 1), oracle.shard_partial(x[4:8], 4, 8, 1)]
+    lp, tok, ok = oracle.merge_shard_partials(parts, 8, 8, 1)
+    assert not ok and tok[1] == 8 and math.isnan(lp[1])
