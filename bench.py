@@ -48,7 +48,10 @@ VARIANT_TEXT = {
     "none": "",
     "temperature": "; per-batch temperatures U[0.25,2] (every 4th exactly 1), logprobs of x/tau",
     "variable": "; VARIABLE logits: only each sequence's last positions present (all for echo, 1-3 otherwise)",
+    "vocab8": "; vocab-parallel over 8 shards, one rank's work on one GPU: partials over its 1/8 of the columns "
+              "+ merge of the 8 gathered tuple slices (the all-gather between GPUs is not in the step)",
 }
+SHARDS = 8
 
 
 def load_batch(config: str, variant: str, dev):
@@ -242,7 +245,8 @@ def run_ours(args, rank: int, world: int, dist):
     B, T_logits, V, levels = batch.B, batch.T, batch.V, batch.levels
     T = batch.tokens.numel()  # input positions (== T_logits unless VARIABLE logits)
     pos_off = batch.positions_offsets
-    extended = args.variant != "none"
+    extended = args.variant in ("temperature", "variable")
+    sharded = args.variant == "vocab8"
     W = lp.out_per_token(levels)
     ws = lp.new_workspace(B, T, V, levels, dev)
     host = torch.zeros(2, dtype=torch.int32).pin_memory()
@@ -254,16 +258,32 @@ def run_ours(args, rank: int, world: int, dist):
     out_lp = torch.empty((R, W), dtype=torch.float32, device=dev)
     out_tok = torch.empty((R, W), dtype=torch.int32, device=dev)
 
+    stream = torch.cuda.current_stream()
+    full_logits = batch.logits
+    if sharded:
+        # Rank 0's columns; the gathered buffer holds every shard's tuples (filled once,
+        # as the all-gather would), so the merge in each step reads all P slices.
+        bounds = [round(i * V / SHARDS) for i in range(SHARDS + 1)]
+        stride = lp.tuple_bytes(levels)
+        gathered = torch.zeros((SHARDS, R * stride), dtype=torch.uint8, device=dev)
+        for p_ in range(SHARDS):
+            lp.shard_partials(batch.logits[:, bounds[p_]:bounds[p_ + 1]].contiguous(), bounds[p_],
+                              batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, out_off, batch.echo,
+                              levels, gathered[p_], R, ws)
+        full_logits = batch.logits[:, bounds[0]:bounds[1]].contiguous()
+
     # Rotate over enough logits copies that each step reads HBM, not L2.
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or (128 << 20))
-    lbytes = batch.logits.numel() * 4
+    lbytes = full_logits.numel() * 4
     n_copies = max(1, math.ceil(3 * l2 / lbytes))
-    copies = [batch.logits] + [batch.logits.clone() for _ in range(n_copies - 1)]
-    stream = torch.cuda.current_stream()
+    copies = [full_logits] + [full_logits.clone() for _ in range(n_copies - 1)]
 
     def launch_compute(logits, loff, ioff, tokens, sampled, echo, tau):
-        if extended:
+        if sharded:
+            lp.shard_partials(logits, 0, loff, tokens, sampled, out_off, echo, levels, gathered[0], R, ws,
+                              stream=stream)
+        elif extended:
             lp.compute_ex(logits, loff, tokens, sampled, out_off, echo, levels, out_lp, out_tok, ws,
                           input_row_offsets=ioff, temperatures=tau, stream=stream)
         else:
@@ -277,6 +297,8 @@ def run_ours(args, rank: int, world: int, dist):
                        batch.sampled_tokens, batch.echo, batch.temperatures)
         if ev is not None:
             ev[1].record(stream)
+        if sharded:
+            lp.shard_merge(gathered, SHARDS, R, V, out_off, levels, out_lp, out_tok, ws, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -343,12 +365,12 @@ def run_ours(args, rank: int, world: int, dist):
     # End to end through the public API: pinned host inputs -> device, plan+compute, results -> host.
     e2e = None
     if not args.no_e2e:
-        h_logits = batch.logits.cpu().pin_memory()
+        h_logits = full_logits.cpu().pin_memory()
         # logits offsets, tokens, sampled, echo, then the variant's inputs (input offsets, temperatures)
         small = [batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, batch.echo]
         small += [t for t in (batch.input_row_offsets, batch.temperatures) if t is not None]
         h_ints = [t.cpu().pin_memory() for t in small]
-        d_logits = torch.empty_like(batch.logits)
+        d_logits = torch.empty_like(full_logits)
         d_ints = [torch.empty_like(t) for t in small]
         d_ioff = d_ints[4] if batch.input_row_offsets is not None else None
         d_tau = d_ints[-1] if batch.temperatures is not None else None
@@ -365,6 +387,8 @@ def run_ours(args, rank: int, world: int, dist):
             lp.plan(d_ioff if d_ioff is not None else d_ints[0], d_ints[3], T, ws, output_row_offsets=out_off,
                     stream=stream)
             launch_compute(d_logits, d_ints[0], d_ioff, d_ints[1], d_ints[2], d_ints[3], d_tau)
+            if sharded:
+                lp.shard_merge(gathered, SHARDS, R, V, out_off, levels, out_lp, out_tok, ws, stream=stream)
             h_lp.copy_(out_lp, non_blocking=True)
             h_tok.copy_(out_tok, non_blocking=True)
 
@@ -394,14 +418,17 @@ def run_ours(args, rank: int, world: int, dist):
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": k_e2e,
                "host_assembly_ms": round(asm_ms, 3)}
 
-    alg = algorithmic_bytes(R, V, W, B)
+    if sharded:  # the partial kernel: its columns read once, one tuple written per row
+        alg = R * full_logits.shape[1] * 4 + R * lp.tuple_bytes(levels) + (B + 1) * 8 + R * 4
+    else:
+        alg = algorithmic_bytes(R, V, W, B)
     achieved = alg / (compute_ms / 1e3) / 1e9
     peak, peak_src = measured_peak_hbm()
     traffic = None
     rec = NCU_TRAFFIC.get(args.config if args.variant == "none" else f"{args.config}/{args.variant}")
     if rec and rec.get("source_hash") == kernel_source_hash():
         traffic = rec["bytes_per_launch"]
-    entry = "lp_ragged_compute_ex" if extended else "lp_ragged_compute"
+    entry = "lp_ragged_shard_partials" if sharded else ("lp_ragged_compute_ex" if extended else "lp_ragged_compute")
     kernel_name = (f"k_rows_cta ({entry}, row queue)" if 2 * min(T, T_logits) < rows_kernel_warps()
                    else f"k_rows ({entry}, warp ranges)")
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
@@ -432,8 +459,12 @@ def run_ours(args, rank: int, world: int, dist):
                          f"(L2 {l2 / 1e6:.0f} MB)"},
         "hbm_gbs_step": round(alg * world / (ms_step / 1e3) / 1e9, 1),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 2 * args.steps, "clocks": clocks,
+        "gpu_launches": (3 if sharded else 2) * args.steps, "clocks": clocks,
     }
+    if sharded:
+        line["config"]["shards"] = SHARDS
+        line["config"]["note"] = ("value = rows/s of one rank's step (partials over V/8 columns + merge); the 8 ranks "
+                                  "run in parallel, so it is the job's rate less the all-gather, untimed on one GPU")
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -159,6 +159,71 @@ lp_status lp_ragged_compute_ex(const float *logits, uint32_t T_logits, uint32_t 
                                lp_stream_t stream);
 
 /*
+ * Vocab-parallel form (the forward pass runs on tensor-parallel workers, SGLang page
+ * "logprob、finish reason 与 output processing", section "第一步：ModelRunner.forward()
+ * 输出 logits"; with the lm_head split by vocabulary each rank holds a contiguous range
+ * of columns). Three steps per rank, on the same inputs except the logits:
+ *   1. lp_ragged_plan (as usual; positions offsets),
+ *   2. lp_ragged_shard_partials: this rank's columns -> one row tuple per output row,
+ *   3. gather all ranks' tuple buffers into one [P][rows_capacity][stride] buffer in
+ *      shard order (e.g. an NCCL all-gather), then lp_ragged_shard_merge -> the rows,
+ *      identical to lp_ragged_compute on the unsplit logits (ids exact; logprobs
+ *      within rounding).
+ *
+ * Row tuple layout (u32 words, stride = lp_ragged_tuple_bytes(levels) bytes, a
+ * multiple of 16):
+ *   [0] c  fp32 reference in the log2 domain: max logit of the shard's row x log2(e)/tau
+ *          (-inf when every column is -inf; NaN marks an invalid row)
+ *   [1] s  fp32 sum over the shard's columns of 2^(x*log2(e)/tau - c)
+ *   [2] fp32 logit of the target token when this shard holds it, else 0
+ *   [3] target token id in bits 0-30 (ids >= 2^31 stored as 2^31-1); bit 31 set when
+ *       this shard holds the target
+ *   [4, 4+K)     the shard's K best fp32 logits, sorted (logit desc, global id asc),
+ *                -inf padding
+ *   [4+K, 4+2K)  their global token ids (vocab_base + column), 0xFFFFFFFF padding
+ */
+uint32_t lp_ragged_tuple_bytes(uint32_t levels);
+
+/*
+ *   logits          device, float[T_logits][V_shard]: this rank's columns
+ *                   [vocab_base, vocab_base + V_shard) of the full vocabulary
+ *   vocab_base      global id of column 0 (vocab_base + V_shard < 2^31 - 1)
+ *   tuples          device out, rows_capacity x lp_ragged_tuple_bytes(levels) bytes,
+ *                   16-byte aligned; rows_capacity >= R, else nothing is written and
+ *                   the LP_ERR_OFFSETS bit is set
+ *   other arguments as lp_ragged_compute_ex (temperatures: the same on every rank).
+ * A token id is not range-checked here (only the merge knows the full vocabulary).
+ * An invalid row (bad offsets or temperature) sets its status bit and gets a tuple
+ * with c = NaN.
+ */
+lp_status lp_ragged_shard_partials(const float *logits, uint32_t T_logits, uint32_t V_shard, uint32_t vocab_base,
+                                   const uint32_t *logit_row_offsets, const uint32_t *input_row_offsets, uint32_t T,
+                                   uint32_t B, const uint32_t *tokens, const uint32_t *sampled_tokens,
+                                   const uint32_t *output_row_offsets, const uint8_t *echo,
+                                   const float *temperatures, uint32_t levels, void *tuples,
+                                   uint32_t rows_capacity, void *workspace, size_t workspace_bytes,
+                                   lp_stream_t stream);
+
+/*
+ *   tuples          device, [P][rows_capacity][stride] bytes: shard p's tuple of output
+ *                   row o at byte (p * rows_capacity + o) * stride. The P shards must
+ *                   cover the vocabulary [0, V) exactly (a target no shard holds gets
+ *                   logprob NaN). rows_capacity >= R, else LP_ERR_OFFSETS bit.
+ *   V               full vocabulary size: targets >= V set LP_ERR_TOKEN_RANGE and get
+ *                   logprob NaN
+ *   output_row_offsets, B   as written by lp_ragged_plan
+ *   temperatures    the same array the shards used, or NULL
+ *   out_logprobs, out_tokens  device out, R x W, as lp_ragged_compute
+ *   workspace       only its status word is used (set bits; plan clears it)
+ * A row any of whose tuples is invalid gets NaN / 0xFFFFFFFF (the shard call set the
+ * status bit). One warp per row; no allocation.
+ */
+lp_status lp_ragged_shard_merge(const void *tuples, uint32_t P, uint32_t rows_capacity, uint32_t V,
+                                const uint32_t *output_row_offsets, uint32_t B, const float *temperatures,
+                                uint32_t levels, float *out_logprobs, uint32_t *out_tokens, void *workspace,
+                                size_t workspace_bytes, lp_stream_t stream);
+
+/*
  * Allocation-free form of lp_ragged_compute (no counterpart on the pages; it exists
  * for callers that cannot allocate device memory: a serving engine whose HBM is
  * reserved up front by its own pool and that forbids cudaMalloc on the request

@@ -22,7 +22,8 @@ from .results import LogProbabilities, assemble  # noqa: F401  (host-side result
 
 __all__ = [
     "LpError", "lib_path", "load", "workspace_size", "new_workspace", "plan", "compute",
-    "compute_ex", "read_status", "ragged_log_probs", "out_per_token", "STATUS_NAMES", "LogProbabilities", "assemble",
+    "compute_ex", "read_status", "ragged_log_probs", "tuple_bytes", "shard_partials", "shard_merge",
+    "gather_shard_tuples", "ragged_log_probs_vocab_parallel", "out_per_token", "STATUS_NAMES", "LogProbabilities", "assemble",
 ]
 
 LP_MAX_LEVELS = 6
@@ -32,6 +33,7 @@ STATUS_NAMES = {
     5: "LP_ERR_TOKEN_RANGE", 6: "LP_ERR_WORKSPACE", 7: "LP_ERR_CUDA", 8: "LP_ERR_TEMPERATURE",
 }
 EXPORTS = ("lp_ragged_workspace_size", "lp_ragged_plan", "lp_ragged_compute", "lp_ragged_compute_ex",
+           "lp_ragged_tuple_bytes", "lp_ragged_shard_partials", "lp_ragged_shard_merge",
            "lp_ragged_read_status", "lp_ragged_strerror")
 
 
@@ -66,6 +68,13 @@ def load() -> ctypes.CDLL:
     lib.lp_ragged_compute.restype = ctypes.c_int
     lib.lp_ragged_compute_ex.argtypes = [vp, u32, u32, vp, vp, u32, u32, vp, vp, vp, vp, vp, u32, vp, vp, vp, sz, vp]
     lib.lp_ragged_compute_ex.restype = ctypes.c_int
+    lib.lp_ragged_tuple_bytes.argtypes = [u32]
+    lib.lp_ragged_tuple_bytes.restype = u32
+    lib.lp_ragged_shard_partials.argtypes = [vp, u32, u32, u32, vp, vp, u32, u32, vp, vp, vp, vp, vp, u32, vp, u32,
+                                             vp, sz, vp]
+    lib.lp_ragged_shard_partials.restype = ctypes.c_int
+    lib.lp_ragged_shard_merge.argtypes = [vp, u32, u32, u32, vp, u32, vp, u32, vp, vp, vp, sz, vp]
+    lib.lp_ragged_shard_merge.restype = ctypes.c_int
     lib.lp_ragged_read_status.argtypes = [vp, vp, vp]
     lib.lp_ragged_read_status.restype = ctypes.c_int
     lib.lp_ragged_strerror.argtypes = [ctypes.c_int]
@@ -213,6 +222,115 @@ def compute_ex(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: to
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc:
         raise LpError(rc, "lp_ragged_compute_ex")
+
+
+def tuple_bytes(levels: int) -> int:
+    """Bytes of one row tuple of the vocab-parallel form (a multiple of 16)."""
+    n = int(load().lp_ragged_tuple_bytes(levels))
+    if n == 0:
+        raise LpError(2, "lp_ragged_tuple_bytes")
+    return n
+
+
+def shard_partials(logits: torch.Tensor, vocab_base: int, logit_row_offsets: torch.Tensor, tokens: torch.Tensor,
+                   sampled_tokens: torch.Tensor, output_row_offsets: torch.Tensor, echo: torch.Tensor, levels: int,
+                   tuples: torch.Tensor, rows_capacity: int, workspace: torch.Tensor,
+                   input_row_offsets: Optional[torch.Tensor] = None, temperatures: Optional[torch.Tensor] = None,
+                   stream=None) -> None:
+    """Enqueue ``lp_ragged_shard_partials``: this rank's vocab columns
+    ``[vocab_base, vocab_base + logits.shape[1])`` -> one row tuple per output row in
+    ``tuples`` (uint8 CUDA tensor of at least ``rows_capacity * tuple_bytes(levels)``)."""
+    lib = load()
+    if logits.dim() != 2 or logits.dtype != torch.float32 or not logits.is_cuda:
+        raise TypeError("logits must be a 2-D float32 CUDA tensor")
+    if logits.stride(1) != 1 or logits.stride(0) != logits.shape[1]:
+        raise ValueError("logits must be row-major contiguous")
+    T_logits, V_shard = logits.shape
+    B = logit_row_offsets.numel() - 1
+    T = tokens.numel()
+    if input_row_offsets is None and T != T_logits:
+        raise ValueError("without input_row_offsets every position needs a logits row")
+    if not tuples.is_cuda or not tuples.is_contiguous() or \
+            tuples.numel() * tuples.element_size() < rows_capacity * tuple_bytes(levels):
+        raise ValueError("tuples must be a contiguous CUDA buffer of rows_capacity * tuple_bytes(levels) bytes")
+    ioff = 0 if input_row_offsets is None else _dev_u32(input_row_offsets, "input_row_offsets", B + 1)
+    tp = 0 if temperatures is None else temperatures.data_ptr()
+    rc = lib.lp_ragged_shard_partials(
+        logits.data_ptr(), T_logits, V_shard, vocab_base, _dev_u32(logit_row_offsets, "logit_row_offsets", B + 1),
+        ioff, T, B, _dev_u32(tokens, "tokens", T), _dev_u32(sampled_tokens, "sampled_tokens", B),
+        _dev_u32(output_row_offsets, "output_row_offsets", B + 1), _dev_u8(echo, "echo", B), tp, levels,
+        tuples.data_ptr(), rows_capacity, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    if rc:
+        raise LpError(rc, "lp_ragged_shard_partials")
+
+
+def shard_merge(tuples: torch.Tensor, P: int, rows_capacity: int, V: int, output_row_offsets: torch.Tensor,
+                levels: int, out_logprobs: torch.Tensor, out_tokens: torch.Tensor, workspace: torch.Tensor,
+                temperatures: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Enqueue ``lp_ragged_shard_merge`` over ``tuples`` = [P][rows_capacity][stride] bytes."""
+    lib = load()
+    B = output_row_offsets.numel() - 1
+    if not tuples.is_cuda or not tuples.is_contiguous() or \
+            tuples.numel() * tuples.element_size() < P * rows_capacity * tuple_bytes(levels):
+        raise ValueError("tuples must hold P * rows_capacity row tuples")
+    tp = 0 if temperatures is None else temperatures.data_ptr()
+    rc = lib.lp_ragged_shard_merge(tuples.data_ptr(), P, rows_capacity, V,
+                                   _dev_u32(output_row_offsets, "output_row_offsets", B + 1), B, tp, levels,
+                                   out_logprobs.data_ptr(), _dev_u32(out_tokens, "out_tokens"), workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc:
+        raise LpError(rc, "lp_ragged_shard_merge")
+
+
+def gather_shard_tuples(local: torch.Tensor, group=None) -> torch.Tensor:
+    """The exchange step of the vocab-parallel form: every rank's tuple buffer (same
+    size on all ranks), concatenated in rank order = shard order, on every rank."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    out = torch.empty((world,) + tuple(local.shape), dtype=local.dtype, device=local.device)
+    if local.is_cuda:
+        dist.all_gather_into_tensor(out, local.contiguous(), group=group)
+    else:  # gloo has no all_gather_into_tensor
+        dist.all_gather(list(out.unbind(0)), local.contiguous(), group=group)
+    return out
+
+
+def ragged_log_probs_vocab_parallel(logits_shard: torch.Tensor, vocab_base: int, vocab_size: int,
+                                    logit_row_offsets: torch.Tensor, tokens: torch.Tensor,
+                                    sampled_tokens: torch.Tensor, echo: torch.Tensor, levels: int, group=None,
+                                    input_row_offsets: Optional[torch.Tensor] = None,
+                                    temperatures: Optional[torch.Tensor] = None, check: bool = True):
+    """One rank of the vocab-parallel form: plan -> shard partials -> all-gather of the
+    tuples (torch.distributed) -> merge. Ranks hold contiguous column ranges in rank
+    order covering [0, vocab_size). Returns the same triple as ``ragged_log_probs``."""
+    T_logits, V_shard = logits_shard.shape
+    B = logit_row_offsets.numel() - 1
+    T = tokens.numel() if input_row_offsets is not None else T_logits
+    pos_off = input_row_offsets if input_row_offsets is not None else logit_row_offsets
+    dev = logits_shard.device
+    workspace = new_workspace(B, T, V_shard, levels, dev)
+    host = torch.zeros(2, dtype=torch.int32).pin_memory()
+    out_off = plan(pos_off, echo, T, workspace, host_out=host)
+    torch.cuda.current_stream().synchronize()
+    R, status = int(host[0]), int(host[1]) & 0xFFFFFFFF
+    if status:
+        raise LpError(_first_bit(status), "lp_ragged_plan (device)")
+    stride = tuple_bytes(levels)
+    local = torch.empty(max(R, 1) * stride, dtype=torch.uint8, device=dev)
+    shard_partials(logits_shard, vocab_base, logit_row_offsets, tokens, sampled_tokens, out_off, echo, levels, local,
+                   max(R, 1), workspace, input_row_offsets=input_row_offsets, temperatures=temperatures)
+    gathered = gather_shard_tuples(local, group)
+    W = out_per_token(levels)
+    out_lp = torch.empty((R, W), dtype=torch.float32, device=dev)
+    out_tok = torch.empty((R, W), dtype=torch.int32, device=dev)
+    shard_merge(gathered, gathered.shape[0], max(R, 1), vocab_size, out_off, levels, out_lp, out_tok, workspace,
+                temperatures=temperatures)
+    if check:
+        status = read_status(workspace)
+        if status:
+            raise LpError(_first_bit(status), "vocab-parallel ragged log-probabilities (device)")
+    return out_off, out_lp, out_tok
 
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:

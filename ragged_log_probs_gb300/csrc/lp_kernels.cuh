@@ -102,7 +102,19 @@ struct RowsParams {
     const uint32_t* loff;    // logits rows per batch: the batch's last positions (== off
                              // when every position has a logits row)
     const float* tau;        // per-batch temperature, or nullptr for raw logits
+    unsigned char* tuple_out;  // vocab shard mode: one row tuple per output row instead of
+                               // logprobs (nullptr: write rows)
+    uint32_t vocab_base;     // vocab shard mode: global id of the shard's column 0
+    uint32_t tuple_rows;     // vocab shard mode: rows the tuple buffer holds
 };
+
+// Row tuple of one vocab shard (lp_ragged_shard_partials), u32 words:
+//   [0] reference c (NaN: the row is invalid)  [1] sum s  [2] target logit
+//   [3] target id (bits 0-30; ids >= 2^31 are stored as 2^31-1) | bit 31: this shard
+//       holds the target
+//   [4, 4+K) top-k logits (sorted)  [4+K, 4+2K) their global ids
+// Same stride as a split-row partial slot.
+constexpr uint32_t kTupleHolds = 0x80000000u;
 
 // ---------------------------------------------------------------------------------
 // Plan: one CTA, chunked block-wide exclusive scan.
@@ -466,6 +478,52 @@ __device__ __forceinline__ void write_row(const RowsParams& p, uint32_t o, const
     }
 }
 
+// An invalid row gets NaN logprobs and padding ids; its status bit is raised.
+__device__ __forceinline__ void write_invalid_row(const RowsParams& p, uint32_t o, uint32_t err, int lane) {
+    for (uint32_t col = (uint32_t)lane; col < p.W; col += 32) {
+        p.out_lp[(size_t)o * p.W + col] = __int_as_float(0x7fc00000);
+        p.out_tok[(size_t)o * p.W + col] = kPadId;
+    }
+    if (lane == 0) atomicOr(p.status, err);
+}
+
+// Vocab shard mode: store a finished row's tuple (ids offset to global ids).
+template <int SLOTS, bool TOPK>
+__device__ __forceinline__ void store_row_tuple(const RowsParams& p, uint32_t o, const WarpList<SLOTS>& L, float C,
+                                                float S, uint32_t t, bool has_xt, float xt, int lane) {
+    uint32_t* pw = reinterpret_cast<uint32_t*>(p.tuple_out + (size_t)o * p.stride);
+    if (lane == 0) {
+        pw[0] = __float_as_uint(C);
+        pw[1] = __float_as_uint(S);
+        pw[2] = __float_as_uint(has_xt ? xt : 0.f);
+        pw[3] = (t < kTupleHolds ? t : kTupleHolds - 1u) | (has_xt ? kTupleHolds : 0u);
+    }
+    if constexpr (TOPK) {
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+            const uint32_t i = (uint32_t)lane + 32u * k;
+            if (i < p.K) {
+                pw[4 + i] = __float_as_uint(L.x[k]);
+                pw[4 + p.K + i] = L.id[k] == kPadId ? kPadId : L.id[k] + p.vocab_base;
+            }
+        }
+    }
+}
+
+// An invalid row: NaN logprobs and padding ids (or, in vocab shard mode, a tuple whose
+// reference is NaN); its status bit is raised.
+template <bool EXT>
+__device__ __forceinline__ void emit_invalid(const RowsParams& p, uint32_t o, uint32_t err, int lane) {
+    if (EXT && p.tuple_out != nullptr) {
+        uint32_t* pw = reinterpret_cast<uint32_t*>(p.tuple_out + (size_t)o * p.stride);
+        for (uint32_t i = (uint32_t)lane; i < 4u + 2u * p.K; i += 32)
+            pw[i] = (i < 4u + p.K) ? 0x7fc00000u : kPadId;
+        if (lane == 0) atomicOr(p.status, err);
+    } else {
+        write_invalid_row(p, o, err, lane);
+    }
+}
+
 // Partial tuple of piece j of a row whose first piece belongs to warp w0. A warp
 // stores the piece of its first row in slot 0 and that of its last row in slot 1;
 // only piece 0 can be its warp's last row.
@@ -600,14 +658,6 @@ __device__ __forceinline__ RowDesc describe_row(const RowsParams& p, const uint3
     return d;
 }
 
-// An invalid row gets NaN logprobs and padding ids; its status bit is raised.
-__device__ __forceinline__ void write_invalid_row(const RowsParams& p, uint32_t o, uint32_t err, int lane) {
-    for (uint32_t col = (uint32_t)lane; col < p.W; col += 32) {
-        p.out_lp[(size_t)o * p.W + col] = __int_as_float(0x7fc00000);
-        p.out_tok[(size_t)o * p.W + col] = kPadId;
-    }
-    if (lane == 0) atomicOr(p.status, err);
-}
 
 // Stage the per-batch arrays in shared memory: [off][out_off][loff if distinct][echo].
 template <bool EXT>
@@ -661,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
     }
     if (status & kStatusOffsets) return;  // plan rejected the offsets
     if (R == 0) return;
-    if (R > p.T) {
+    if (R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusOffsets);
         return;
     }
@@ -693,20 +743,21 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
         // ---- row descriptor (identical in every lane) ---------------------------------
         const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, b, o);
         if (d.err) {
-            if (q0 == 0) write_invalid_row(p, o, d.err, lane);
+            if (q0 == 0) emit_invalid<EXT>(p, o, d.err, lane);
         } else {
             const uint32_t t = d.t;
+            const uint32_t t_loc = EXT ? t - p.vocab_base : t;  // column of the target in this shard
             const float* rowp = d.rowp;
             const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
             const int64_t e_lo = 4 * (int64_t)q0 - a, e_hi = 4 * (int64_t)q1 - a;
-            const bool t_here = t < V && (int64_t)t >= e_lo && (int64_t)t < e_hi;
+            const bool t_here = t_loc < V && (int64_t)t_loc >= e_lo && (int64_t)t_loc < e_hi;
 
             LaneSum ls;
             ls.init(d.k);
             Selector<SLOTS> sel;
             sel.init(s_cx[w], s_ci[w], K);
             float xt = 0.f;
-            stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, q0, q1, lane, ls, sel, t_here, t, xt, ring);
+            stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, q0, q1, lane, ls, sel, t_here, t_loc, xt, ring);
 
             float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, S = ls.s;
             warp_lse2_reduce(C, S);
@@ -729,7 +780,12 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
                     if (lane == 0) p.counters[w0] = 0u;  // ready for the next call
                 }
             }
-            if (emit) write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, has_xt, xt_row, d.k, lane);
+            if (emit) {
+                if (EXT && p.tuple_out != nullptr)
+                    store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, S, t, has_xt, xt_row, lane);
+                else
+                    write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, has_xt, xt_row, d.k, lane);
+            }
         }
 
         // ---- next piece -----------------------------------------------------------
@@ -786,7 +842,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo);
     if (threadIdx.x == 0) { cm.has_xt = 0u; cm.thr = 0u; }
     uint32_t* queue = p.counters;  // [0] next row, [1] CTAs finished, [2 + sm] CTAs of that SM
-    bool bad = (status & kStatusOffsets) || R > p.T;
+    const bool too_many = R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows);
+    bool bad = (status & kStatusOffsets) || too_many;
     if (threadIdx.x == 0) {
         uint32_t smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -797,7 +854,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     __syncthreads();
     const bool takes_part = cm.row != 0;
     __syncthreads();
-    if (threadIdx.x == 0 && blockIdx.x == 0 && R > p.T && !(status & kStatusOffsets))
+    if (threadIdx.x == 0 && blockIdx.x == 0 && too_many && !(status & kStatusOffsets))
         atomicOr(p.status, kStatusOffsets);
     float4* ring = rings + (size_t)w * STAGES * U * 32;
 
@@ -813,24 +870,25 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         }
         const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, lo, o);
         if (d.err) {
-            if (w == 0) write_invalid_row(p, o, d.err, lane);
+            if (w == 0) emit_invalid<EXT>(p, o, d.err, lane);
             __syncthreads();
             continue;
         }
         const uint32_t t = d.t;
+        const uint32_t t_loc = EXT ? t - p.vocab_base : t;  // column of the target in this shard
         const float* rowp = d.rowp;
         const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
         const uint32_t wq0 = (uint32_t)(((uint64_t)p.nq * w) / NW);
         const uint32_t wq1 = (uint32_t)(((uint64_t)p.nq * (w + 1)) / NW);
         const int64_t e_lo = 4 * (int64_t)wq0 - a, e_hi = 4 * (int64_t)wq1 - a;
-        const bool t_here = t < V && (int64_t)t >= e_lo && (int64_t)t < e_hi;
+        const bool t_here = t_loc < V && (int64_t)t_loc >= e_lo && (int64_t)t_loc < e_hi;
 
         LaneSum ls;
         ls.init(d.k);
         Selector<SLOTS> sel;
         sel.init(s_cx[w], s_ci[w], K);
         float xt = 0.f;
-        stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t, xt, ring, &cm.thr);
+        stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr);
 
         float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, S = ls.s;
         warp_lse2_reduce(C, S);
@@ -873,7 +931,10 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             S = 0.f;
             for (int j = lane; j < NW; j += 32) lse2_combine(C, S, cm.red_c[j], cm.red_s[j]);
             warp_lse2_reduce(C, S);
-            write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, d.k, lane);
+            if (EXT && p.tuple_out != nullptr)
+                store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, lane);
+            else
+                write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, d.k, lane);
             __syncwarp();
             if (lane == 0) { cm.has_xt = 0u; cm.thr = 0u; }
         }
@@ -886,6 +947,71 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             queue[1] = 0u;
             for (uint32_t i = 0; i < p.num_sms; ++i) queue[2 + i] = 0u;
         }
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// Vocab shard merge: P row tuples per output row (one per vocab shard, as gathered from
+// the ranks) -> the row's logprobs. One warp per row: the shards' (reference, sum)
+// pairs combine in the log2 domain, their sorted top-k lists merge in shard order
+// under (logit desc, global id asc), and the target logit comes from the shard that
+// holds it.
+constexpr int kMergeWarps = 8;
+
+template <int SLOTS, bool TOPK>
+__global__ void __launch_bounds__(kMergeWarps * 32) k_shard_merge(RowsParams p, const unsigned char* tuples,
+                                                                  uint32_t P, uint32_t rows_capacity) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t R = __ldg(p.out_off + p.B);
+    if (R > rows_capacity) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusOffsets);
+        return;
+    }
+    const size_t shard_bytes = (size_t)rows_capacity * p.stride;
+    const uint32_t nw = gridDim.x * kMergeWarps;
+    for (uint32_t o = blockIdx.x * kMergeWarps + (threadIdx.x >> 5); o < R; o += nw) {
+        const unsigned char* row0 = tuples + (size_t)o * p.stride;
+        float C = neg_inf(), S = 0.f, xt = 0.f;
+        bool has_xt = false, bad = false;
+        uint32_t t = 0;
+        for (uint32_t j = (uint32_t)lane; j < P; j += 32) {
+            const uint32_t* hw = reinterpret_cast<const uint32_t*>(row0 + j * shard_bytes);
+            const float hc = __uint_as_float(__ldg(hw)), hs = __uint_as_float(__ldg(hw + 1));
+            const uint32_t w3 = __ldg(hw + 3);
+            if (hc != hc) bad = true;
+            else lse2_combine(C, S, hc, hs);
+            if (w3 & kTupleHolds) { xt = __uint_as_float(__ldg(hw + 2)); has_xt = true; }
+            t = w3 & ~kTupleHolds;
+        }
+        if (__any_sync(kFull, bad)) {
+            write_invalid_row(p, o, 0u, lane);
+            continue;
+        }
+        warp_lse2_reduce(C, S);
+        const unsigned hb = __ballot_sync(kFull, has_xt);
+        has_xt = hb != 0;
+        xt = __shfl_sync(kFull, xt, hb ? __ffs(hb) - 1 : 0);
+        t = __shfl_sync(kFull, t, 0);
+        WarpList<SLOTS> L;
+        L.reset();
+        if constexpr (TOPK) {
+            for (uint32_t j = 0; j < P; ++j) {
+                float cx[SLOTS];
+                uint32_t ci[SLOTS];
+                load_piece_list<SLOTS>(reinterpret_cast<const uint32_t*>(row0 + j * shard_bytes), p.K, lane, cx, ci);
+                merge_lists<SLOTS>(L.x, L.id, cx, ci, lane);
+            }
+        }
+        float kk = kLog2e;
+        if (p.tau != nullptr) {  // same scale as the shards used (validated there)
+            uint32_t lo = 0, hi = p.B;
+            while (hi - lo > 1) {
+                const uint32_t mid = (lo + hi) >> 1;
+                if (__ldg(p.out_off + mid) <= o) lo = mid; else hi = mid;
+            }
+            kk = __fdiv_rn(kLog2e, __ldg(p.tau + lo));
+        }
+        write_row<SLOTS, TOPK>(p, o, L, C, S, t, has_xt, xt, kk, lane);
     }
 }
 

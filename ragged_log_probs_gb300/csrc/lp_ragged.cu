@@ -163,14 +163,16 @@ lp_status lp_ragged_plan(const uint32_t* logit_row_offsets, const uint8_t* echo,
     return LP_OK;
 }
 
-lp_status lp_ragged_compute_ex(const float* logits, uint32_t T_logits, uint32_t V,
-                               const uint32_t* logit_row_offsets, const uint32_t* input_row_offsets, uint32_t T,
-                               uint32_t B, const uint32_t* tokens, const uint32_t* sampled_tokens,
-                               const uint32_t* output_row_offsets, const uint8_t* echo, const float* temperatures,
-                               uint32_t levels, float* out_logprobs, uint32_t* out_tokens, void* workspace,
-                               size_t workspace_bytes, lp_stream_t stream) {
+// The row kernels' launch: writes rows (tuples == nullptr) or, for a vocab shard,
+// one row tuple per output row with ids offset by vocab_base.
+static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V, const uint32_t* logit_row_offsets,
+                              const uint32_t* input_row_offsets, uint32_t T, uint32_t B, const uint32_t* tokens,
+                              const uint32_t* sampled_tokens, const uint32_t* output_row_offsets, const uint8_t* echo,
+                              const float* temperatures, uint32_t levels, float* out_logprobs, uint32_t* out_tokens,
+                              void* tuples, uint32_t vocab_base, uint32_t tuple_rows, void* workspace,
+                              size_t workspace_bytes, lp_stream_t stream) {
     if (!logits || !logit_row_offsets || !tokens || !sampled_tokens || !output_row_offsets || !echo ||
-        !out_logprobs || !out_tokens)
+        (!tuples && (!out_logprobs || !out_tokens)))
         return LP_ERR_NULL;
     if (!workspace) return LP_ERR_WORKSPACE;
     if (levels > LP_MAX_LEVELS) return LP_ERR_LEVELS;
@@ -193,6 +195,9 @@ lp_status lp_ragged_compute_ex(const float* logits, uint32_t T_logits, uint32_t 
     p.off = input_row_offsets ? input_row_offsets : logit_row_offsets;
     p.loff = logit_row_offsets;
     p.tau = temperatures;
+    p.tuple_out = static_cast<unsigned char*>(tuples);
+    p.vocab_base = vocab_base;
+    p.tuple_rows = tuple_rows;
     p.tokens = tokens;
     p.sampled = sampled_tokens;
     p.out_off = output_row_offsets;
@@ -223,7 +228,7 @@ lp_status lp_ragged_compute_ex(const float* logits, uint32_t T_logits, uint32_t 
     // half the warps; otherwise warp-owned ranges of the row space (the two kernels give
     // the same result).
     // Plain instantiation unless an extended input is given (it compiles without them).
-    const bool ext = input_row_offsets != nullptr || temperatures != nullptr;
+    const bool ext = input_row_offsets != nullptr || temperatures != nullptr || tuples != nullptr;
     int v = variant_of(levels) + (ext ? 6 : 0);
     int occ = occupancy(d, v, smem);
     if (occ == 0) return LP_ERR_CUDA;
@@ -263,14 +268,85 @@ lp_status lp_ragged_compute_ex(const float* logits, uint32_t T_logits, uint32_t 
     return LP_OK;
 }
 
+lp_status lp_ragged_compute_ex(const float* logits, uint32_t T_logits, uint32_t V,
+                               const uint32_t* logit_row_offsets, const uint32_t* input_row_offsets, uint32_t T,
+                               uint32_t B, const uint32_t* tokens, const uint32_t* sampled_tokens,
+                               const uint32_t* output_row_offsets, const uint8_t* echo, const float* temperatures,
+                               uint32_t levels, float* out_logprobs, uint32_t* out_tokens, void* workspace,
+                               size_t workspace_bytes, lp_stream_t stream) {
+    return compute_impl(logits, T_logits, V, logit_row_offsets, input_row_offsets, T, B, tokens, sampled_tokens,
+                        output_row_offsets, echo, temperatures, levels, out_logprobs, out_tokens, nullptr, 0u, 0u,
+                        workspace, workspace_bytes, stream);
+}
+
 lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const uint32_t* logit_row_offsets,
                             uint32_t B, const uint32_t* tokens, const uint32_t* sampled_tokens,
                             const uint32_t* output_row_offsets, const uint8_t* echo, uint32_t levels,
                             float* out_logprobs, uint32_t* out_tokens, void* workspace, size_t workspace_bytes,
                             lp_stream_t stream) {
-    return lp_ragged_compute_ex(logits, T, V, logit_row_offsets, nullptr, T, B, tokens, sampled_tokens,
-                                output_row_offsets, echo, nullptr, levels, out_logprobs, out_tokens, workspace,
-                                workspace_bytes, stream);
+    return compute_impl(logits, T, V, logit_row_offsets, nullptr, T, B, tokens, sampled_tokens, output_row_offsets,
+                        echo, nullptr, levels, out_logprobs, out_tokens, nullptr, 0u, 0u, workspace,
+                        workspace_bytes, stream);
+}
+
+uint32_t lp_ragged_tuple_bytes(uint32_t levels) {
+    return levels > LP_MAX_LEVELS ? 0u : lpk::partial_stride_bytes((1u << levels) - 1u);
+}
+
+lp_status lp_ragged_shard_partials(const float* logits, uint32_t T_logits, uint32_t V_shard, uint32_t vocab_base,
+                                   const uint32_t* logit_row_offsets, const uint32_t* input_row_offsets, uint32_t T,
+                                   uint32_t B, const uint32_t* tokens, const uint32_t* sampled_tokens,
+                                   const uint32_t* output_row_offsets, const uint8_t* echo,
+                                   const float* temperatures, uint32_t levels, void* tuples,
+                                   uint32_t rows_capacity, void* workspace, size_t workspace_bytes,
+                                   lp_stream_t stream) {
+    if (!tuples) return LP_ERR_NULL;
+    if (rows_capacity == 0) return LP_ERR_SHAPE;
+    if (((uintptr_t)tuples & 15u) != 0) return LP_ERR_SHAPE;
+    if ((uint64_t)vocab_base + V_shard >= 0x7FFFFFFFull) return LP_ERR_SHAPE;
+    return compute_impl(logits, T_logits, V_shard, logit_row_offsets, input_row_offsets, T, B, tokens,
+                        sampled_tokens, output_row_offsets, echo, temperatures, levels, nullptr, nullptr, tuples,
+                        vocab_base, rows_capacity, workspace, workspace_bytes, stream);
+}
+
+lp_status lp_ragged_shard_merge(const void* tuples, uint32_t P, uint32_t rows_capacity, uint32_t V,
+                                const uint32_t* output_row_offsets, uint32_t B, const float* temperatures,
+                                uint32_t levels, float* out_logprobs, uint32_t* out_tokens, void* workspace,
+                                size_t workspace_bytes, lp_stream_t stream) {
+    if (!tuples || !output_row_offsets || !out_logprobs || !out_tokens) return LP_ERR_NULL;
+    if (!workspace || workspace_bytes < sizeof(lpk::WsHeader)) return LP_ERR_WORKSPACE;
+    if (((uintptr_t)workspace & 255u) != 0) return LP_ERR_WORKSPACE;
+    if (levels > LP_MAX_LEVELS) return LP_ERR_LEVELS;
+    if (P == 0 || B == 0 || V == 0 || V >= 0x7FFFFFFFu || rows_capacity == 0) return LP_ERR_SHAPE;
+    if (((uintptr_t)tuples & 15u) != 0) return LP_ERR_SHAPE;
+    int dev;
+    DeviceInfo* d;
+    if (!device_info(&dev, &d)) return LP_ERR_CUDA;
+    lpk::RowsParams p = {};
+    p.out_off = output_row_offsets;
+    p.tau = temperatures;
+    p.out_lp = out_logprobs;
+    p.out_tok = out_tokens;
+    p.status = &static_cast<lpk::WsHeader*>(workspace)->status;
+    p.B = B;
+    p.V = V;
+    p.K = (1u << levels) - 1u;
+    p.W = levels ? (1u << levels) : 1u;
+    p.stride = lpk::partial_stride_bytes(p.K);
+    const uint32_t per_cta = lpk::kMergeWarps;
+    uint32_t grid = (rows_capacity + per_cta - 1) / per_cta;
+    const uint32_t cap = (uint32_t)d->sms * 4u;
+    if (grid > cap) grid = cap;
+    const auto* tp = static_cast<const unsigned char*>(tuples);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (levels == 0)
+        lpk::k_shard_merge<1, false><<<grid, per_cta * 32, 0, s>>>(p, tp, P, rows_capacity);
+    else if (levels < 6)
+        lpk::k_shard_merge<1, true><<<grid, per_cta * 32, 0, s>>>(p, tp, P, rows_capacity);
+    else
+        lpk::k_shard_merge<2, true><<<grid, per_cta * 32, 0, s>>>(p, tp, P, rows_capacity);
+    if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
+    return LP_OK;
 }
 
 lp_status lp_ragged_read_status(const void* workspace, uint32_t* host_status, lp_stream_t stream) {

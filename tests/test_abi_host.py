@@ -89,6 +89,30 @@ def test_compute_ex_host_checks(lib):
     assert _compute_ex(lib, ws=FAKE + 64) == LP_ERR_WORKSPACE
 
 
+def test_shard_entry_points_host_checks(lib):
+    assert lib.lp_ragged_tuple_bytes(3) == 80 and lib.lp_ragged_tuple_bytes(6) == 528
+    assert lib.lp_ragged_tuple_bytes(0) == 16 and lib.lp_ragged_tuple_bytes(7) == 0
+    part = lambda **kw: lib.lp_ragged_shard_partials(
+        kw.get("logits", FAKE), 4, kw.get("V", 100), kw.get("base", 0), FAKE, None, 4, 2, FAKE, FAKE, FAKE, FAKE,
+        None, kw.get("levels", 3), kw.get("tuples", FAKE), kw.get("cap", 8), FAKE, 1 << 20, None)
+    assert part(tuples=None) == LP_ERR_NULL
+    assert part(tuples=FAKE + 8) == LP_ERR_SHAPE
+    assert part(cap=0) == LP_ERR_SHAPE
+    assert part(base=0x7FFFFFF0, V=100) == LP_ERR_SHAPE
+    assert part(logits=None) == LP_ERR_NULL
+    assert part(levels=7) == LP_ERR_LEVELS
+    merge = lambda **kw: lib.lp_ragged_shard_merge(
+        kw.get("tuples", FAKE), kw.get("P", 2), kw.get("cap", 8), kw.get("V", 100), FAKE, 2, None,
+        kw.get("levels", 3), FAKE, FAKE, kw.get("ws", FAKE), 1 << 20, None)
+    assert merge(tuples=None) == LP_ERR_NULL
+    assert merge(ws=None) == LP_ERR_WORKSPACE
+    assert merge(levels=7) == LP_ERR_LEVELS
+    assert merge(P=0) == LP_ERR_SHAPE
+    assert merge(V=0) == LP_ERR_SHAPE
+    assert merge(cap=0) == LP_ERR_SHAPE
+    assert merge(tuples=FAKE + 4) == LP_ERR_SHAPE
+
+
 def test_plan_host_checks(lib):
     plan = lib.lp_ragged_plan
     assert plan(None, FAKE, 2, 4, FAKE, None, FAKE, 1 << 20, None) == LP_ERR_NULL
