@@ -309,10 +309,18 @@ __device__ __forceinline__ float4 load_checked(const float* rowp, const float* v
 // Full blocks (U vectors per lane, 512*U contiguous bytes per warp) go through a ring
 // of STAGES blocks in shared memory filled by cp.async, so STAGES-1 blocks stay in
 // flight while one is reduced; each lane reads back only what it copied itself.
-template <int SLOTS, bool TOPK, int U, int STAGES>
+//
+// TABW > 0 (row-queue kernel: TABW warps stream parts of the same row): at each
+// threshold refresh the warp publishes its lanes' running maxima in lane_tab[w][lane]
+// and bounds the top-k by the K-th largest over lanes of max_j lane_tab[j][lane]. Each
+// of those 32 values is an element of a different (warp, lane) stream of the row, so K
+// of them are K distinct elements, and with TABW times more elements behind each value
+// the bound sits much closer to the row's true K-th best than one warp's own.
+template <int SLOTS, bool TOPK, int U, int STAGES, int TABW = 0>
 __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint32_t q0, uint32_t q1, int lane,
                                              LaneSum& ls, Selector<SLOTS>& sel, bool t_here, uint32_t t,
-                                             float& xt, float4* ring, uint32_t* shared_thr = nullptr) {
+                                             float& xt, float4* ring, uint32_t* shared_thr = nullptr,
+                                             float* lane_tab = nullptr, int w = 0) {
     const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
     const float* vbase = rowp - a;  // 16-byte aligned
     const uint32_t qf = a ? 1u : 0u;
@@ -371,7 +379,14 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
             // threshold that follows the warp's true K-th best at the cost of one float
             // sort, refreshed on the first block and then every kThrEvery blocks.
             if ((blk & (kThrEvery - 1)) == 0) {
-                sel.thr = fmaxf(sel.thr, kth_largest32(ls.m, sel.K, lane));
+                float lm = ls.m;
+                if constexpr (TABW > 0) {
+                    volatile float* tab = lane_tab;
+                    tab[w * 32 + lane] = lm;
+#pragma unroll
+                    for (int j = 0; j < TABW; ++j) lm = fmaxf(lm, tab[j * 32 + lane]);
+                }
+                sel.thr = fmaxf(sel.thr, kth_largest32(lm, sel.K, lane));
                 if (shared_thr != nullptr) {  // warps on the same row share their thresholds
                     if (lane == 0 && sel.thr != neg_inf()) atomicMax(shared_thr, f2ord(sel.thr));
                     sel.thr = fmaxf(sel.thr, ord2f(*(volatile uint32_t*)shared_thr));
@@ -803,7 +818,8 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
 // merged in shared memory, so no row goes through global partials or tickets. At most
 // ceil(R / SMs) CTAs of an SM take part (a per-SM slot counter), so all rows stream at
 // once and no SM carries more than its share. The last CTA to leave resets the queue
-// words and the per-SM counters for the next call.
+// words and the per-SM counters for the next call. The warps of a CTA also share their
+// lanes' running maxima for the top-k threshold (see stream_piece).
 template <int NW>
 struct CtaMerge {
     float list_x[NW][64];
@@ -814,6 +830,7 @@ struct CtaMerge {
     uint32_t has_xt;
     uint32_t row;
     uint32_t thr;  // threshold shared by the warps of the CTA for the current row
+    float lane_max[NW][32];  // running lane maxima of the current row (-inf between rows)
 };
 
 constexpr int kQueueWarps = LP_QUEUE_WARPS;
@@ -840,27 +857,46 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const uint32_t* out_off = p.out_off;
     const uint8_t* echo = p.echo;
     if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo);
-    if (threadIdx.x == 0) { cm.has_xt = 0u; cm.thr = 0u; }
-    uint32_t* queue = p.counters;  // [0] next row, [1] CTAs finished, [2 + sm] CTAs of that SM
+    cm.lane_max[w][lane] = neg_inf();
+    // Row hand-out. [0] next row of the first queue (rows [0, nA), one per SM), [1] CTAs
+    // finished, [2 + sm] CTAs seen on that SM, [2 + SMs] next row of the second queue
+    // (rows [nA, R)). At most ceil(R / SMs) CTAs of an SM take part; an SM's first one
+    // takes one row of the first queue, then every participant drains the second queue
+    // and then the first, so every SM carries one or two rows' worth before any SM gets a
+    // third, and no row is left behind if an SM gets fewer CTAs.
+    uint32_t* queue = p.counters;
+    const uint32_t nA = R < p.num_sms ? R : p.num_sms;
     const bool too_many = R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows);
-    bool bad = (status & kStatusOffsets) || too_many;
+    const bool bad = (status & kStatusOffsets) || too_many;
+    auto next_row = [&]() -> uint32_t {  // thread 0 only
+        const uint32_t rb = nA + atomicAdd(queue + 2 + p.num_sms, 1u);
+        if (rb < R) return rb;
+        const uint32_t ra = atomicAdd(queue, 1u);
+        return ra < nA ? ra : R;
+    };
     if (threadIdx.x == 0) {
-        uint32_t smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        const uint32_t slot = atomicAdd(queue + 2 + smid % p.num_sms, 1u);
-        const uint32_t cap = p.num_sms ? (R + p.num_sms - 1) / p.num_sms : 1u;
-        cm.row = slot < cap ? 1u : 0u;  // this CTA takes part
+        cm.has_xt = 0u;
+        cm.thr = 0u;
+        uint32_t row = R;
+        if (!bad) {
+            uint32_t smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            const uint32_t slot = atomicAdd(queue + 2 + smid % p.num_sms, 1u);
+            const uint32_t cap = p.num_sms ? (R + p.num_sms - 1) / p.num_sms : 1u;
+            if (slot == 0) {
+                const uint32_t ra = atomicAdd(queue, 1u);
+                row = ra < nA ? ra : next_row();
+            } else if (slot < cap) {
+                row = next_row();
+            }
+        }
+        cm.row = row;
+        if (blockIdx.x == 0 && too_many && !(status & kStatusOffsets)) atomicOr(p.status, kStatusOffsets);
     }
-    __syncthreads();
-    const bool takes_part = cm.row != 0;
-    __syncthreads();
-    if (threadIdx.x == 0 && blockIdx.x == 0 && too_many && !(status & kStatusOffsets))
-        atomicOr(p.status, kStatusOffsets);
     float4* ring = rings + (size_t)w * STAGES * U * 32;
+    __syncthreads();
 
     for (;;) {
-        if (threadIdx.x == 0) cm.row = (bad || !takes_part) ? R : atomicAdd(queue, 1u);
-        __syncthreads();
         const uint32_t o = cm.row;
         if (o >= R) break;
         uint32_t lo = 0, hi = B;  // batch of row o
@@ -871,6 +907,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, lo, o);
         if (d.err) {
             if (w == 0) emit_invalid<EXT>(p, o, d.err, lane);
+            __syncthreads();  // every thread has read cm.row
+            if (threadIdx.x == 0) cm.row = next_row();
             __syncthreads();
             continue;
         }
@@ -888,7 +926,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         Selector<SLOTS> sel;
         sel.init(s_cx[w], s_ci[w], K);
         float xt = 0.f;
-        stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr);
+        stream_piece<SLOTS, TOPK, U, STAGES, NW>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr,
+                                                 &cm.lane_max[0][0], w);
 
         float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, S = ls.s;
         warp_lse2_reduce(C, S);
@@ -936,8 +975,13 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             else
                 write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, d.k, lane);
             __syncwarp();
-            if (lane == 0) { cm.has_xt = 0u; cm.thr = 0u; }
+            if (lane == 0) {
+                cm.has_xt = 0u;
+                cm.thr = 0u;
+                cm.row = next_row();  // every thread read cm.row before the merge barriers
+            }
         }
+        cm.lane_max[w][lane] = neg_inf();  // every warp is past its row's stream
         __syncthreads();
     }
     if (threadIdx.x == 0) {
@@ -945,7 +989,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {  // last CTA out: ready for the next call
             queue[0] = 0u;
             queue[1] = 0u;
-            for (uint32_t i = 0; i < p.num_sms; ++i) queue[2 + i] = 0u;
+            for (uint32_t i = 0; i <= p.num_sms; ++i) queue[2 + i] = 0u;
         }
     }
 }
