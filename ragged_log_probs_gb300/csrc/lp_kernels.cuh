@@ -56,7 +56,10 @@ namespace lpk {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr uint32_t kThrEvery = 4;  // blocks between lane-maximum threshold refreshes (power of 2)
+#ifndef LP_THR_EVERY
+#define LP_THR_EVERY 8
+#endif
+constexpr uint32_t kThrEvery = LP_THR_EVERY;  // blocks between lane-maximum threshold refreshes (power of 2)
 constexpr int kPlanThreads = 1024;
 constexpr uint32_t kStatusOffsets = 1u << 4;     // bit of LP_ERR_OFFSETS
 constexpr uint32_t kStatusTokenRange = 1u << 5;  // bit of LP_ERR_TOKEN_RANGE
