@@ -208,3 +208,25 @@ def test_top_elements_in_one_lane_misaligned(V):
     x[1, :] = 0.25
     x[2, 1:9] = 50.0
     parity.check_batch(_custom(x, [6], [1], 3, seed=V), what=f"one-lane-misaligned/{V}")
+
+
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
+def test_compute_twice_after_one_plan(kernel, monkeypatch):
+    # The row kernels leave their queue and ticket words cleared, so a second compute on
+    # the same plan (no plan in between) gives the same rows, bit for bit (both kernels
+    # split rows statically: the summation order does not depend on timing).
+    monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
+    b = workloads.make_next_token_batch(40, 150001, levels=3, device="cuda", seed=21)
+    ws = lp.new_workspace(b.B, b.T, b.V, b.levels)
+    out_off = lp.plan(b.logit_row_offsets, b.echo, b.T, ws)
+    outs = []
+    for _ in range(3):
+        o_lp = torch.empty((b.B, 8), device="cuda")
+        o_tok = torch.empty((b.B, 8), dtype=torch.int32, device="cuda")
+        lp.compute(b.logits, b.logit_row_offsets, b.tokens, b.sampled_tokens, out_off, b.echo, 3, o_lp, o_tok, ws)
+        assert lp.read_status(ws) == 0
+        outs.append((o_lp.cpu().numpy(), o_tok.cpu().numpy()))
+    for lp_, tok_ in outs[1:]:
+        assert np.array_equal(tok_, outs[0][1]) and np.array_equal(lp_, outs[0][0])
+    ref = parity.oracle_for(b)
+    parity.compare(outs[0][0], outs[0][1].view(np.uint32).astype(np.uint64), ref[1], ref[2], "twice")
