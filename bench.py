@@ -66,9 +66,9 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 135530752, "source_hash": "46fbf212b89b4868",
+    "decode": {"bytes_per_launch": 134867968, "source_hash": "fb7df4011e79f4d5",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 904372224, "source_hash": "46fbf212b89b4868",
+    "prefill": {"bytes_per_launch": 904280320, "source_hash": "fb7df4011e79f4d5",
                 "capture": "profiles/k_rows_prefill.md"},
 }
 
@@ -81,11 +81,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def rows_kernel_warps() -> int:
-    """Warps of the warp-range kernel's grid (152 SMs x 3 CTAs x 8 warps on GB300);
-    the library picks the row-queue kernel when 2*T is below this."""
+def queue_rows_limit() -> int:
+    """The library runs the row-queue kernel when at most this many rows can come out
+    (two per SM: 304 on GB300), else the warp-range kernel."""
     import torch
-    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count * 3 * 8
+    return 2 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
 
 
 def algorithmic_bytes(R: int, V: int, W: int, B: int) -> int:
@@ -279,26 +279,38 @@ def run_ours(args, rank: int, world: int, dist):
     n_copies = max(1, math.ceil(3 * l2 / lbytes))
     copies = [full_logits] + [full_logits.clone() for _ in range(n_copies - 1)]
 
-    def launch_compute(logits, loff, ioff, tokens, sampled, echo, tau):
+    def launch_compute(logits, loff, ioff, tokens, sampled, echo, tau, st=None):
+        st = stream if st is None else st
         if sharded:
             lp.shard_partials(logits, 0, loff, tokens, sampled, out_off, echo, levels, gathered[0], R, ws,
-                              stream=stream)
+                              stream=st)
         elif extended:
             lp.compute_ex(logits, loff, tokens, sampled, out_off, echo, levels, out_lp, out_tok, ws,
-                          input_row_offsets=ioff, temperatures=tau, stream=stream)
+                          input_row_offsets=ioff, temperatures=tau, stream=st)
         else:
-            lp.compute(logits, loff, tokens, sampled, out_off, echo, levels, out_lp, out_tok, ws, stream=stream)
+            lp.compute(logits, loff, tokens, sampled, out_off, echo, levels, out_lp, out_tok, ws, stream=st)
 
-    def step(i, ev=None):
-        lp.plan(pos_off, batch.echo, T, ws, output_row_offsets=out_off, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
+    def step(i, st=None):
+        st = stream if st is None else st
+        lp.plan(pos_off, batch.echo, T, ws, output_row_offsets=out_off, stream=st)
         launch_compute(copies[i % n_copies], batch.logit_row_offsets, batch.input_row_offsets, batch.tokens,
-                       batch.sampled_tokens, batch.echo, batch.temperatures)
-        if ev is not None:
-            ev[1].record(stream)
+                       batch.sampled_tokens, batch.echo, batch.temperatures, st)
         if sharded:
-            lp.shard_merge(gathered, SHARDS, R, V, out_off, levels, out_lp, out_tok, ws, stream=stream)
+            lp.shard_merge(gathered, SHARDS, R, V, out_off, levels, out_lp, out_tok, ws, stream=st)
+
+    def capture(n, body):
+        """n calls of body(k, stream) captured in one CUDA graph (launch-bound loops replay
+        without host launch overhead; the library's launches carry their programmatic
+        dependencies into the graph)."""
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(g, stream=cs):
+                for k in range(n):
+                    body(k, cs)
+        stream.wait_stream(cs)
+        return g
 
     for i in range(args.warmup):
         step(i)
@@ -319,15 +331,26 @@ def run_ours(args, rank: int, world: int, dist):
         uuid = u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         pass
+    # The timed K steps (plan + compute, inputs rotating) and, for the kernel's own
+    # duration, n_ev compute launches alone, each captured once in a CUDA graph (after the
+    # eager warm-up above, which also did the library's one-time setup).
+    g_steps = capture(args.steps, lambda k, st: step(k, st))
+    n_ev = max(20, min(args.steps, 500))
+    g_compute = capture(n_ev, lambda k, st: launch_compute(
+        copies[k % n_copies], batch.logit_row_offsets, batch.input_row_offsets, batch.tokens,
+        batch.sampled_tokens, batch.echo, batch.temperatures, st))
+    g_steps.replay()
+    g_compute.replay()
+    torch.cuda.synchronize()
+    if lp.read_status(ws) != 0:
+        raise RuntimeError("device status set during the graph warm-up")
+
     sampler = ClockSampler(uuid)
     sampler.start()
     # untimed settle so the clock samples see the GPU under load
     t_settle = time.perf_counter()
-    i = 0
     while time.perf_counter() - t_settle < args.settle_s:
-        for _ in range(50):
-            step(i)
-            i += 1
+        g_steps.replay()
         torch.cuda.synchronize()
 
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -336,8 +359,7 @@ def run_ours(args, rank: int, world: int, dist):
     torch.cuda.synchronize()
     w0 = time.time()
     t_start.record(stream)
-    for k in range(args.steps):
-        step(k)
+    g_steps.replay()
     t_end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
@@ -345,17 +367,14 @@ def run_ours(args, rank: int, world: int, dist):
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
     ms_step = ms_total / args.steps
-    # Per-launch duration of the row kernel: the same step loop again, with an event pair
-    # around every compute launch. Kept out of the timed region above because an event
-    # between the plan and the compute launch stops the compute kernel from starting
-    # while the plan runs (programmatic dependent launch).
-    n_ev = max(20, min(args.steps, 500))
-    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
-    for k in range(n_ev):
-        step(k, events[k])
+    # Per-launch duration of the row kernel: n_ev compute launches back to back.
+    c_start, c_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c_start.record(stream)
+    g_compute.replay()
+    c_end.record(stream)
     torch.cuda.synchronize()
     sampler.stop()
-    compute_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
+    compute_ms = c_start.elapsed_time(c_end) / n_ev
     ms_step, compute_ms = combine_over_ranks([ms_step, compute_ms], dist, dev)
     clocks = sampler.summary(w0, w1)
     status = lp.read_status(ws)
@@ -429,10 +448,11 @@ def run_ours(args, rank: int, world: int, dist):
     if rec and rec.get("source_hash") == kernel_source_hash():
         traffic = rec["bytes_per_launch"]
     entry = "lp_ragged_shard_partials" if sharded else ("lp_ragged_compute_ex" if extended else "lp_ragged_compute")
-    kernel_name = (f"k_rows_cta ({entry}, row queue)" if 2 * min(T, T_logits) < rows_kernel_warps()
+    kernel_name = (f"k_rows_cta ({entry}, row queue)" if min(T, T_logits) <= queue_rows_limit()
                    else f"k_rows ({entry}, warp ranges)")
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
-                "timing": f"CUDA events around each of {n_ev} compute launches, same stream, right after the timed steps",
+                "timing": f"CUDA events around one CUDA-graph replay of {n_ev} back-to-back compute launches, same "
+                          f"stream, right after the timed steps",
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
@@ -456,7 +476,8 @@ def run_ours(args, rank: int, world: int, dist):
                    "variant": args.variant, "B": B, "T": T, "T_logits": T_logits, "V": V,
                    "levels": levels, "rows_per_gpu": R, "parallelism": f"replicas x{world} (independent batches)",
                    "l2": f"inputs larger than L2: {n_copies} rotating logits copies of {lbytes / 1e6:.0f} MB "
-                         f"(L2 {l2 / 1e6:.0f} MB)"},
+                         f"(L2 {l2 / 1e6:.0f} MB)",
+                   "launch": "the K timed steps (plan + compute each) replayed from one CUDA graph"},
         "hbm_gbs_step": round(alg * world / (ms_step / 1e3) / 1e9, 1),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (3 if sharded else 2) * args.steps, "clocks": clocks,

@@ -109,6 +109,8 @@ struct RowsParams {
                                // logprobs (nullptr: write rows)
     uint32_t vocab_base;     // vocab shard mode: global id of the shard's column 0
     uint32_t tuple_rows;     // vocab shard mode: rows the tuple buffer holds
+    uint32_t split;          // row-queue kernel: pieces per row (1: whole rows)
+    uint32_t split_rows;     // row-queue kernel: rows the workspace holds tickets and pieces for
 };
 
 // Row tuple of one vocab shard (lp_ragged_shard_partials), u32 words:
@@ -621,11 +623,11 @@ __device__ __forceinline__ void merge_pieces(const RowsParams& p, uint64_t w0, u
 }
 
 // Publish a piece and take a ticket; true for the warp that arrives last.
-__device__ __forceinline__ bool take_ticket(const RowsParams& p, uint64_t w0, uint32_t pieces, int lane) {
+__device__ __forceinline__ bool take_ticket(uint32_t* counters, uint64_t w0, uint32_t pieces, int lane) {
     __threadfence();
     __syncwarp();
     uint32_t ticket = 0;
-    if (lane == 0) ticket = atomicAdd(p.counters + w0, 1u);
+    if (lane == 0) ticket = atomicAdd(counters + w0, 1u);
     ticket = __shfl_sync(kFull, ticket, 0);
     const bool last = ticket == pieces - 1;
     if (last) __threadfence();
@@ -734,7 +736,10 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
         return;
     }
     const uint64_t Q = (uint64_t)R * p.nq;
+    // pieces of at least min_piece vectors, but at least one warp per row: short rows
+    // would otherwise queue up behind a few warps, each paying a row's fixed costs
     uint64_t G = (Q + p.min_piece - 1) / p.min_piece;
+    if (G < R) G = R;
     const uint64_t G_launch = (uint64_t)gridDim.x * kWarps;
     if (G > G_launch) G = G_launch;
     if (G == 0) G = 1;
@@ -791,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
                 store_piece<SLOTS, TOPK>(reinterpret_cast<uint32_t*>(
                                              p.partials + (size_t)(2 * gw + (o == o_first ? 0 : 1)) * p.stride),
                                          K, sel.L, C, S, has_xt, xt_row, lane);
-                emit = take_ticket(p, w0, pieces, lane);
+                emit = take_ticket(p.counters, w0, pieces, lane);
                 if (emit) {
                     const bool tail0 = sk_start(w0, Q, G) != gr;
                     merge_pieces<SLOTS, TOPK>(p, w0, pieces, tail0, lane, sel.L, C, S, has_xt, xt_row);
@@ -815,14 +820,18 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
 }
 
 // ---------------------------------------------------------------------------------
-// Few rows (each row much larger than a warp's share, e.g. next-token logits for a
-// decode batch): CTAs of NW warps take whole rows from a queue (one atomic counter)
-// and split each row into NW contiguous parts, one per warp; the warps' results are
-// merged in shared memory, so no row goes through global partials or tickets. At most
-// ceil(R / SMs) CTAs of an SM take part (a per-SM slot counter), so all rows stream at
-// once and no SM carries more than its share. The last CTA to leave resets the queue
-// words and the per-SM counters for the next call. The warps of a CTA also share their
-// lanes' running maxima for the top-k threshold (see stream_piece).
+// Few rows (at most two per SM, e.g. next-token logits for a decode batch): CTAs of NW
+// warps take tasks from a queue (atomic counters); a task is a whole row, or, when there
+// are fewer rows than twice the SMs, one of S contiguous pieces of a row (split-vocab:
+// S = min(2*SMs / rows, row length / 16 KB, 64), chosen on the host). The CTA's warps
+// split the task into NW contiguous parts and merge their results in shared memory; a
+// whole row is written at once, a piece is published to the workspace and the CTA that
+// takes the row's last ticket merges the S pieces with all its warps (each warp merges
+// every NW-th piece, then the shared-memory tree). At most ceil(tasks / SMs) CTAs of an
+// SM take part (a per-SM slot counter), so all tasks stream at once and no SM carries
+// more than its share. The warps of a CTA share their lanes' running maxima for the
+// top-k threshold (see stream_piece). The last CTA to leave resets the queue words and
+// the per-SM counters for the next call; the merging CTA resets its row's ticket.
 template <int NW>
 struct CtaMerge {
     float list_x[NW][64];
@@ -833,6 +842,7 @@ struct CtaMerge {
     uint32_t has_xt;
     uint32_t row;
     uint32_t thr;  // threshold shared by the warps of the CTA for the current row
+    uint32_t last;  // this CTA took the last ticket of its split row
     float lane_max[NW][32];  // running lane maxima of the current row (-inf between rows)
 };
 
@@ -861,89 +871,57 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const uint8_t* echo = p.echo;
     if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo);
     cm.lane_max[w][lane] = neg_inf();
-    // Row hand-out. [0] next row of the first queue (rows [0, nA), one per SM), [1] CTAs
-    // finished, [2 + sm] CTAs seen on that SM, [2 + SMs] next row of the second queue
-    // (rows [nA, R)). At most ceil(R / SMs) CTAs of an SM take part; an SM's first one
-    // takes one row of the first queue, then every participant drains the second queue
-    // and then the first, so every SM carries one or two rows' worth before any SM gets a
-    // third, and no row is left behind if an SM gets fewer CTAs.
+    // Tasks: piece `task % S` of row `task / S` (S = p.split pieces per row). Hand-out:
+    // [0] next task of the first queue (tasks [0, nA), one per SM), [1] CTAs finished,
+    // [2 + sm] CTAs seen on that SM, [2 + SMs] next task of the second queue (tasks
+    // [nA, R*S)); with S > 1, one arrival ticket per row from [3 + SMs]. At most
+    // ceil(R*S / SMs) CTAs of an SM take part; an SM's first one takes one task of the
+    // first queue, then every participant drains the second queue and then the first, so
+    // every SM carries one or two tasks before any SM gets a third, and no task is left
+    // behind if an SM gets fewer CTAs.
+    const uint32_t S = p.split;
     uint32_t* queue = p.counters;
-    const uint32_t nA = R < p.num_sms ? R : p.num_sms;
-    const bool too_many = R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows);
+    uint32_t* tickets = queue + 3 + p.num_sms;
+    const bool too_many = R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows) ||
+                          (S > 1 && R > p.split_rows);
     const bool bad = (status & kStatusOffsets) || too_many;
-    auto next_row = [&]() -> uint32_t {  // thread 0 only
+    const uint32_t ntask = bad ? 0u : R * S;
+    const uint32_t nA = ntask < p.num_sms ? ntask : p.num_sms;
+    auto next_task = [&]() -> uint32_t {  // thread 0 only
         const uint32_t rb = nA + atomicAdd(queue + 2 + p.num_sms, 1u);
-        if (rb < R) return rb;
+        if (rb < ntask) return rb;
         const uint32_t ra = atomicAdd(queue, 1u);
-        return ra < nA ? ra : R;
+        return ra < nA ? ra : ntask;
     };
     if (threadIdx.x == 0) {
         cm.has_xt = 0u;
         cm.thr = 0u;
-        uint32_t row = R;
-        if (!bad) {
+        uint32_t task = ntask;
+        if (ntask) {
             uint32_t smid;
             asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
             const uint32_t slot = atomicAdd(queue + 2 + smid % p.num_sms, 1u);
-            const uint32_t cap = p.num_sms ? (R + p.num_sms - 1) / p.num_sms : 1u;
+            const uint32_t cap = p.num_sms ? (ntask + p.num_sms - 1) / p.num_sms : 1u;
             if (slot == 0) {
                 const uint32_t ra = atomicAdd(queue, 1u);
-                row = ra < nA ? ra : next_row();
+                task = ra < nA ? ra : next_task();
             } else if (slot < cap) {
-                row = next_row();
+                task = next_task();
             }
         }
-        cm.row = row;
+        cm.row = task;
         if (blockIdx.x == 0 && too_many && !(status & kStatusOffsets)) atomicOr(p.status, kStatusOffsets);
     }
     float4* ring = rings + (size_t)w * STAGES * U * 32;
     __syncthreads();
 
-    for (;;) {
-        const uint32_t o = cm.row;
-        if (o >= R) break;
-        uint32_t lo = 0, hi = B;  // batch of row o
-        while (hi - lo > 1) {
-            const uint32_t mid = (lo + hi) >> 1;
-            if (out_off[mid] <= o) lo = mid; else hi = mid;
-        }
-        const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, lo, o);
-        if (d.err) {
-            if (w == 0) emit_invalid<EXT>(p, o, d.err, lane);
-            __syncthreads();  // every thread has read cm.row
-            if (threadIdx.x == 0) cm.row = next_row();
-            __syncthreads();
-            continue;
-        }
-        const uint32_t t = d.t;
-        const uint32_t t_loc = EXT ? t - p.vocab_base : t;  // column of the target in this shard
-        const float* rowp = d.rowp;
-        const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
-        const uint32_t wq0 = (uint32_t)(((uint64_t)p.nq * w) / NW);
-        const uint32_t wq1 = (uint32_t)(((uint64_t)p.nq * (w + 1)) / NW);
-        const int64_t e_lo = 4 * (int64_t)wq0 - a, e_hi = 4 * (int64_t)wq1 - a;
-        const bool t_here = t_loc < V && (int64_t)t_loc >= e_lo && (int64_t)t_loc < e_hi;
-
-        LaneSum ls;
-        ls.init(d.k);
-        Selector<SLOTS> sel;
-        sel.init(s_cx[w], s_ci[w], K);
-        float xt = 0.f;
-        stream_piece<SLOTS, TOPK, U, STAGES, NW>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr,
-                                                 &cm.lane_max[0][0], w);
-
-        float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, S = ls.s;
-        warp_lse2_reduce(C, S);
-        if (lane == 0) {
-            cm.red_c[w] = C;
-            cm.red_s[w] = S;
-            if (t_here) { cm.xt = xt; cm.has_xt = 1u; }
-        }
+    // The warps' sorted lists (in cm.list_*) merged into warp 0's list by a shared-memory tree.
+    auto tree_merge = [&](WarpList<SLOTS>& L) {
         if constexpr (TOPK) {
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
-                cm.list_x[w][lane + 32 * k] = sel.L.x[k];
-                cm.list_i[w][lane + 32 * k] = sel.L.id[k];
+                cm.list_x[w][lane + 32 * k] = L.x[k];
+                cm.list_i[w][lane + 32 * k] = L.id[k];
             }
         }
         __syncthreads();
@@ -958,34 +936,137 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                         bx[k] = cm.list_x[w + st][lane + 32 * k];
                         bi[k] = cm.list_i[w + st][lane + 32 * k];
                     }
-                    merge_lists<SLOTS>(sel.L.x, sel.L.id, bx, bi, lane);
+                    merge_lists<SLOTS>(L.x, L.id, bx, bi, lane);
 #pragma unroll
                     for (int k = 0; k < SLOTS; ++k) {
-                        cm.list_x[w][lane + 32 * k] = sel.L.x[k];
-                        cm.list_i[w][lane + 32 * k] = sel.L.id[k];
+                        cm.list_x[w][lane + 32 * k] = L.x[k];
+                        cm.list_i[w][lane + 32 * k] = L.id[k];
                     }
                 }
                 __syncthreads();
             }
         }
+    };
+
+    for (;;) {
+        const uint32_t task = cm.row;
+        if (task >= ntask) break;
+        const uint32_t o = task / S, piece = task - o * S;
+        uint32_t lo = 0, hi = B;  // batch of row o
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (out_off[mid] <= o) lo = mid; else hi = mid;
+        }
+        const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, lo, o);
+        if (d.err) {
+            if (w == 0 && piece == 0) emit_invalid<EXT>(p, o, d.err, lane);
+            __syncthreads();  // every thread has read cm.row
+            if (threadIdx.x == 0) cm.row = next_task();
+            __syncthreads();
+            continue;
+        }
+        const uint32_t t = d.t;
+        const uint32_t t_loc = EXT ? t - p.vocab_base : t;  // column of the target in this shard
+        const float* rowp = d.rowp;
+        const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
+        const uint32_t pq0 = (uint32_t)(((uint64_t)p.nq * piece) / S);
+        const uint32_t pq1 = (uint32_t)(((uint64_t)p.nq * (piece + 1)) / S);
+        const uint32_t wq0 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * w) / NW);
+        const uint32_t wq1 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * (w + 1)) / NW);
+        const int64_t e_lo = 4 * (int64_t)wq0 - a, e_hi = 4 * (int64_t)wq1 - a;
+        const bool t_here = t_loc < V && (int64_t)t_loc >= e_lo && (int64_t)t_loc < e_hi;
+
+        LaneSum ls;
+        ls.init(d.k);
+        Selector<SLOTS> sel;
+        sel.init(s_cx[w], s_ci[w], K);
+        float xt = 0.f;
+        stream_piece<SLOTS, TOPK, U, STAGES, NW>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr,
+                                                 &cm.lane_max[0][0], w);
+
+        float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, Sm = ls.s;
+        warp_lse2_reduce(C, Sm);
+        if (lane == 0) {
+            cm.red_c[w] = C;
+            cm.red_s[w] = Sm;
+            if (t_here) { cm.xt = xt; cm.has_xt = 1u; }
+        }
+        tree_merge(sel.L);
         if (w == 0) {
             C = neg_inf();
-            S = 0.f;
-            for (int j = lane; j < NW; j += 32) lse2_combine(C, S, cm.red_c[j], cm.red_s[j]);
-            warp_lse2_reduce(C, S);
-            if (EXT && p.tuple_out != nullptr)
-                store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, lane);
-            else
-                write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, cm.has_xt != 0, cm.xt, d.k, lane);
+            Sm = 0.f;
+            for (int j = lane; j < NW; j += 32) lse2_combine(C, Sm, cm.red_c[j], cm.red_s[j]);
+            warp_lse2_reduce(C, Sm);
+            uint32_t last = 0u;
+            if (S == 1) {
+                if (EXT && p.tuple_out != nullptr)
+                    store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, lane);
+                else
+                    write_row<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, d.k, lane);
+            } else {
+                // a piece of a split row: publish it; the CTA that takes the row's last
+                // ticket merges all pieces
+                store_piece<SLOTS, TOPK>(
+                    reinterpret_cast<uint32_t*>(p.partials + (size_t)(o * S + piece) * p.stride), K, sel.L, C, Sm,
+                    cm.has_xt != 0, cm.xt, lane);
+                last = take_ticket(tickets, o, S, lane) ? 1u : 0u;
+            }
             __syncwarp();
             if (lane == 0) {
                 cm.has_xt = 0u;
                 cm.thr = 0u;
-                cm.row = next_row();  // every thread read cm.row before the merge barriers
+                cm.last = last;
+                cm.row = next_task();  // every thread read cm.row before the merge barriers
             }
         }
-        cm.lane_max[w][lane] = neg_inf();  // every warp is past its row's stream
+        cm.lane_max[w][lane] = neg_inf();  // every warp is past this task's stream
         __syncthreads();
+        if (S > 1 && cm.last) {
+            // ---- merge the row's S pieces with the whole CTA -----------------------------
+            const unsigned char* base = p.partials + (size_t)o * S * p.stride;
+            C = neg_inf();
+            Sm = 0.f;
+            bool has = false;
+            float xr = 0.f;
+            for (uint32_t j = threadIdx.x; j < S; j += kT) {
+                const uint32_t* hw = reinterpret_cast<const uint32_t*>(base + (size_t)j * p.stride);
+                lse2_combine(C, Sm, __uint_as_float(__ldcg(hw)), __uint_as_float(__ldcg(hw + 1)));
+                if (__ldcg(hw + 3)) { xr = __uint_as_float(__ldcg(hw + 2)); has = true; }
+            }
+            warp_lse2_reduce(C, Sm);
+            if (lane == 0) {
+                cm.red_c[w] = C;
+                cm.red_s[w] = Sm;
+            }
+            if (has) { cm.xt = xr; cm.has_xt = 1u; }  // one piece holds the target
+            sel.L.reset();
+            if constexpr (TOPK) {
+                for (uint32_t j = (uint32_t)w; j < S; j += NW) {
+                    float cx[SLOTS];
+                    uint32_t ci[SLOTS];
+                    load_piece_list<SLOTS>(reinterpret_cast<const uint32_t*>(base + (size_t)j * p.stride), K, lane,
+                                           cx, ci);
+                    merge_lists<SLOTS>(sel.L.x, sel.L.id, cx, ci, lane);
+                }
+            }
+            tree_merge(sel.L);
+            if (w == 0) {
+                C = neg_inf();
+                Sm = 0.f;
+                for (int j = lane; j < NW; j += 32) lse2_combine(C, Sm, cm.red_c[j], cm.red_s[j]);
+                warp_lse2_reduce(C, Sm);
+                if (EXT && p.tuple_out != nullptr)
+                    store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, lane);
+                else
+                    write_row<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, d.k, lane);
+                __syncwarp();
+                if (lane == 0) {
+                    tickets[o] = 0u;  // ready for the next call
+                    cm.has_xt = 0u;
+                }
+            }
+            __syncthreads();
+        }
     }
     if (threadIdx.x == 0) {
         __threadfence();

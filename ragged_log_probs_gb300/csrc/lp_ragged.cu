@@ -18,6 +18,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kMaxCtasPerSm = 4;           // launch cap; sizes the workspace
 constexpr uint32_t kMinPieceVec = 1024;         // 16 KB of logits per warp at least
+constexpr uint32_t kMinSplitVec = 1024;         // 16 KB of logits per row-queue piece at least
+constexpr uint32_t kMaxSplit = 64;              // pieces per row in the row-queue kernel
 constexpr uint32_t kStageOffsetsMax = 2048;     // stage off/out_off in smem when B+1 <= this
 constexpr uint32_t kUnroll = LP_UNROLL;
 constexpr uint32_t kStages = LP_STAGES;
@@ -219,14 +221,22 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     p.min_piece = kMinPieceVec;
     p.stage_offsets = (B + 1u <= kStageOffsetsMax) ? 1u : 0u;
     p.num_sms = (uint32_t)d->sms;
+    p.split = 1;
+    {
+        // rows the row-queue kernel holds a ticket (after its 3 + SMs queue words) and
+        // kMaxSplit piece slots for
+        const uint32_t by_words = g_max - 3u - (uint32_t)d->sms;
+        const uint32_t by_slots = 2u * g_max / kMaxSplit;
+        p.split_rows = by_words < by_slots ? by_words : by_slots;
+    }
 
     const uint32_t staged_arrays = (p.loff != p.off) ? 3u : 2u;
     const size_t smem =
         kRingBytes + (p.stage_offsets ? (size_t)staged_arrays * (B + 1u) * sizeof(uint32_t) + ((B + 3u) & ~3u) : 0);
 
-    // Row queue when even all-echo input (R <= T, and R <= T_logits) gives fewer rows than
-    // half the warps; otherwise warp-owned ranges of the row space (the two kernels give
-    // the same result).
+    // Row queue when even all-echo input (R <= T, and R <= T_logits) gives at most two
+    // rows per SM; otherwise warp-owned ranges of the row space (the two kernels give the
+    // same result).
     // Plain instantiation unless an extended input is given (it compiles without them).
     const bool ext = input_row_offsets != nullptr || temperatures != nullptr || tuples != nullptr;
     int v = variant_of(levels) + (ext ? 6 : 0);
@@ -235,7 +245,7 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;  // occ <= kMaxCtasPerSm
     const char* force = std::getenv("LP_RAGGED_KERNEL");  // test hook: "warp" or "queue"
     const uint32_t r_max = T < T_logits ? T : T_logits;
-    bool queue = 2ull * r_max < (uint64_t)grid * lpk::kWarps;
+    bool queue = r_max <= 2u * (uint32_t)d->sms;
     if (force && std::strcmp(force, "warp") == 0) queue = false;
     if (force && std::strcmp(force, "queue") == 0) queue = true;
     size_t launch_smem = smem;
@@ -249,6 +259,16 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
         occ = occupancy(d, v, launch_smem);
         if (occ == 0) return LP_ERR_CUDA;
         grid = (uint32_t)d->sms * (uint32_t)occ;
+        // split-vocab for small batches: pieces per row so that the tasks fill two per SM
+        uint32_t S = (2u * (uint32_t)d->sms) / (r_max ? r_max : 1u);
+        const uint32_t by_len = p.nq / kMinSplitVec;
+        if (S > by_len) S = by_len;
+        if (S > kMaxSplit) S = kMaxSplit;
+        const char* fs = std::getenv("LP_RAGGED_SPLIT");  // test hook: pieces per row
+        if (fs) S = (uint32_t)std::strtoul(fs, nullptr, 10);
+        if (S < 1) S = 1;
+        if (S > kMaxSplit) S = kMaxSplit;
+        p.split = S;
     }
     // Launched as a programmatic dependent of the previous kernel on the stream (normally
     // lp_ragged_plan): its CTAs become resident while the plan runs and wait on device.

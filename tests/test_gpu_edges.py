@@ -230,3 +230,26 @@ def test_compute_twice_after_one_plan(kernel, monkeypatch):
         assert np.array_equal(tok_, outs[0][1]) and np.array_equal(lp_, outs[0][0])
     ref = parity.oracle_for(b)
     parity.compare(outs[0][0], outs[0][1].view(np.uint32).astype(np.uint64), ref[1], ref[2], "twice")
+
+
+@pytest.mark.parametrize("split", [1, 2, 7, 64])
+@pytest.mark.parametrize("B,V,levels", [(1, 128256, 3), (5, 20011, 6), (13, 111, 3), (40, 50000, 0), (3, 9999, 1)])
+def test_split_vocab_pieces(split, B, V, levels, monkeypatch):
+    # Row-queue kernel with each row cut into `split` pieces (more pieces than vectors
+    # leaves some empty), merged by the CTA that takes the row's last ticket.
+    monkeypatch.setenv("LP_RAGGED_KERNEL", "queue")
+    monkeypatch.setenv("LP_RAGGED_SPLIT", str(split))
+    b = workloads.make_next_token_batch(B, V, levels=levels, dist="normal", scale=3.0, device="cuda",
+                                        seed=B * 31 + split)
+    parity.check_batch(b, what=f"split={split} B={B} V={V} levels={levels}")
+
+
+@pytest.mark.parametrize("split", [3, 17])
+def test_split_vocab_pieces_echo_and_variants(split, monkeypatch):
+    monkeypatch.setenv("LP_RAGGED_KERNEL", "queue")
+    monkeypatch.setenv("LP_RAGGED_SPLIT", str(split))
+    b = workloads.make_batch("mixed", "cuda", B=6, max_len=9, V=30011, seed=90 + split)
+    parity.check_batch(b, what=f"mixed split={split}")
+    bv = workloads.with_temperatures(workloads.make_batch("mixed", "cuda", B=6, max_len=9, V=30011,
+                                                          variable_extra=2, seed=91), seed=split)
+    parity.check_batch(bv, what=f"variable+tau split={split}")
