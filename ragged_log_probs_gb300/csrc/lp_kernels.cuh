@@ -187,23 +187,33 @@ __device__ __forceinline__ uint64_t sk_owner(uint64_t v, uint64_t Q, uint64_t G)
 
 // Per-lane running sum in the log2 domain.
 struct LaneSum {
-    float m;  // largest logit seen (-inf: none)
-    float c;  // reference, m * k rounded (0 while m is -inf)
-    float s;  // sum of 2^(x * k - c)
-    float k;  // log2(e) / temperature
-    __device__ __forceinline__ void init(float scale) { m = neg_inf(); c = 0.f; s = 0.f; k = scale; }
+    float m;   // largest logit seen (-inf: none)
+    float nc;  // minus the reference c = m * k rounded (0 while m is -inf)
+    float2 s;  // sum of 2^(x * k - c), in two halves (packed adds)
+    float k;   // log2(e) / temperature
+    __device__ __forceinline__ void init(float scale) {
+        m = neg_inf();
+        nc = 0.f;
+        s = make_float2(0.f, 0.f);
+        k = scale;
+    }
+    __device__ __forceinline__ float ref() const { return -nc; }
+    __device__ __forceinline__ float sum() const { return s.x + s.y; }
     __device__ __forceinline__ void raise(float nm) {
-        const float nc = nm * k;
-        s = (s == 0.f) ? 0.f : s * ex2(c - nc);
-        c = nc;
+        const float c_new = nm * k;
+        if (s.x != 0.f || s.y != 0.f) {
+            const float f = ex2(-nc - c_new);
+            s = ffma2(s, make_float2(f, f), make_float2(0.f, 0.f));
+        }
+        nc = -c_new;
         m = nm;
     }
-    // Terms of four logits: two packed FMAs, four EX2, one packed add.
-    __device__ __forceinline__ float2 term4(const float4& v) const {
-        const float2 l2e = make_float2(k, k), mc = make_float2(-c, -c);
+    // Add the terms of four logits: two packed FMAs, four EX2, two packed adds.
+    __device__ __forceinline__ void add4(const float4& v) {
+        const float2 l2e = make_float2(k, k), mc = make_float2(nc, nc);
         const float2 y0 = ffma2(make_float2(v.x, v.y), l2e, mc);
         const float2 y1 = ffma2(make_float2(v.z, v.w), l2e, mc);
-        return fadd2(make_float2(ex2(y0.x), ex2(y0.y)), make_float2(ex2(y1.x), ex2(y1.y)));
+        s = fadd2(s, fadd2(make_float2(ex2(y0.x), ex2(y0.y)), make_float2(ex2(y1.x), ex2(y1.y))));
     }
 };
 
@@ -373,10 +383,8 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
         for (int u = 1; u + 1 < U; u += 2) bm = max3(bm, mu[u], mu[u + 1]);
         if ((U & 1) == 0) bm = fmaxf(bm, mu[U - 1]);
         if (bm > ls.m) ls.raise(bm);
-        float2 acc = ls.term4(v[0]);
 #pragma unroll
-        for (int u = 1; u < U; ++u) acc = fadd2(acc, ls.term4(v[u]));
-        ls.s += acc.x + acc.y;
+        for (int u = 0; u < U; ++u) ls.add4(v[u]);
 
         if constexpr (TOPK && SLOTS == 1) {
             // The K-th largest of the 32 lanes' running maxima is the value of K distinct
@@ -399,7 +407,10 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
             }
             if (__any_sync(kFull, bm >= sel.thr)) {
 #pragma unroll
-                for (int u = 0; u < U; ++u) sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr), lane);
+                for (int u = 0; u < U; ++u) {
+                    if (__any_sync(kFull, mu[u] >= sel.thr))
+                        sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr), lane);
+                }
             }
         }
         if constexpr (TOPK && SLOTS == 2) {
@@ -458,8 +469,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
             if (q < hi) v = load_checked(rowp, vbase, q, a, V, qf, nfull, vm);
             const float mx = max4(v);
             if (mx > ls.m) ls.raise(mx);
-            const float2 tt = ls.term4(v);
-            ls.s += tt.x + tt.y;
+            ls.add4(v);
             if constexpr (TOPK) {
                 if (__any_sync(kFull, mx >= sel.thr))
                     sel.append(v, 4u * q - (uint32_t)a, ge_mask(v, sel.thr) & vm, lane);
@@ -782,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
             float xt = 0.f;
             stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, q0, q1, lane, ls, sel, t_here, t_loc, xt, ring);
 
-            float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, S = ls.s;
+            float C = (ls.m == neg_inf()) ? neg_inf() : ls.ref(), S = ls.sum();
             warp_lse2_reduce(C, S);
             bool has_xt = t_here;
             float xt_row = __shfl_sync(kFull, xt, 0);
@@ -984,7 +994,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         stream_piece<SLOTS, TOPK, U, STAGES, NW>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr,
                                                  &cm.lane_max[0][0], w);
 
-        float C = (ls.m == neg_inf()) ? neg_inf() : ls.c, Sm = ls.s;
+        float C = (ls.m == neg_inf()) ? neg_inf() : ls.ref(), Sm = ls.sum();
         warp_lse2_reduce(C, Sm);
         if (lane == 0) {
             cm.red_c[w] = C;
