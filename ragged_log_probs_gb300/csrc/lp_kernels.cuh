@@ -98,7 +98,7 @@ struct RowsParams {
     uint32_t stride;         // partial slot bytes
     uint32_t min_piece;      // minimum vectors per warp
     uint32_t stage_offsets;  // 1: copy off / out_off / echo to shared memory
-    uint32_t num_sms;        // SMs of the device (row-queue kernel: rows per SM cap)
+    uint32_t num_sms;        // SMs of the device (row-queue kernel: tasks started without a queue)
     // Extended inputs (read only by the EXT instantiations; kept last so the fields above
     // keep their parameter offsets):
     uint32_t T_logits;       // rows of logits
@@ -881,44 +881,30 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const uint8_t* echo = p.echo;
     if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo);
     cm.lane_max[w][lane] = neg_inf();
-    // Tasks: piece `task % S` of row `task / S` (S = p.split pieces per row). Hand-out:
-    // [0] next task of the first queue (tasks [0, nA), one per SM), [1] CTAs finished,
-    // [2 + sm] CTAs seen on that SM, [2 + SMs] next task of the second queue (tasks
-    // [nA, R*S)); with S > 1, one arrival ticket per row from [3 + SMs]. At most
-    // ceil(R*S / SMs) CTAs of an SM take part; an SM's first one takes one task of the
-    // first queue, then every participant drains the second queue and then the first, so
-    // every SM carries one or two tasks before any SM gets a third, and no task is left
-    // behind if an SM gets fewer CTAs.
+    // Tasks: piece `task % S` of row `task / S` (S = p.split pieces per row). The launch
+    // holds two CTAs per SM and the first min(tasks, SMs) CTAs (one per SM in the
+    // hardware's dispatch order) start on task blockIdx.x without an atomic; every later
+    // task comes from a queue: [0] next task of [nA, R*S), [1] CTAs finished; with S > 1,
+    // one arrival ticket per row from [2]. Any CTA may take any task, so the result does
+    // not depend on where CTAs land, only the balance does.
     const uint32_t S = p.split;
     uint32_t* queue = p.counters;
-    uint32_t* tickets = queue + 3 + p.num_sms;
+    uint32_t* tickets = queue + 2;
     const bool too_many = R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows) ||
                           (S > 1 && R > p.split_rows);
     const bool bad = (status & kStatusOffsets) || too_many;
     const uint32_t ntask = bad ? 0u : R * S;
     const uint32_t nA = ntask < p.num_sms ? ntask : p.num_sms;
     auto next_task = [&]() -> uint32_t {  // thread 0 only
-        const uint32_t rb = nA + atomicAdd(queue + 2 + p.num_sms, 1u);
-        if (rb < ntask) return rb;
-        const uint32_t ra = atomicAdd(queue, 1u);
-        return ra < nA ? ra : ntask;
+        const uint32_t rb = nA + atomicAdd(queue, 1u);
+        return rb < ntask ? rb : ntask;
     };
     if (threadIdx.x == 0) {
         cm.has_xt = 0u;
         cm.thr = 0u;
         uint32_t task = ntask;
-        if (ntask) {
-            uint32_t smid;
-            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-            const uint32_t slot = atomicAdd(queue + 2 + smid % p.num_sms, 1u);
-            const uint32_t cap = p.num_sms ? (ntask + p.num_sms - 1) / p.num_sms : 1u;
-            if (slot == 0) {
-                const uint32_t ra = atomicAdd(queue, 1u);
-                task = ra < nA ? ra : next_task();
-            } else if (slot < cap) {
-                task = next_task();
-            }
-        }
+        if (blockIdx.x < nA) task = blockIdx.x;
+        else if (ntask > nA) task = next_task();
         cm.row = task;
         if (blockIdx.x == 0 && too_many && !(status & kStatusOffsets)) atomicOr(p.status, kStatusOffsets);
     }
@@ -1083,7 +1069,6 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {  // last CTA out: ready for the next call
             queue[0] = 0u;
             queue[1] = 0u;
-            for (uint32_t i = 0; i <= p.num_sms; ++i) queue[2 + i] = 0u;
         }
     }
 }

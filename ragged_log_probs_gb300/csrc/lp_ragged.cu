@@ -223,9 +223,9 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     p.num_sms = (uint32_t)d->sms;
     p.split = 1;
     {
-        // rows the row-queue kernel holds a ticket (after its 3 + SMs queue words) and
-        // kMaxSplit piece slots for
-        const uint32_t by_words = g_max - 3u - (uint32_t)d->sms;
+        // rows the row-queue kernel holds a ticket (after its 2 queue words) and kMaxSplit
+        // piece slots for
+        const uint32_t by_words = g_max - 2u;
         const uint32_t by_slots = 2u * g_max / kMaxSplit;
         p.split_rows = by_words < by_slots ? by_words : by_slots;
     }
