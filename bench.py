@@ -66,9 +66,9 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 134867968, "source_hash": "fb7df4011e79f4d5",
+    "decode": {"bytes_per_launch": 135173120, "source_hash": "d494a3c2f2d6de1f",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 904280320, "source_hash": "fb7df4011e79f4d5",
+    "prefill": {"bytes_per_launch": 904192768, "source_hash": "d494a3c2f2d6de1f",
                 "capture": "profiles/k_rows_prefill.md"},
 }
 
