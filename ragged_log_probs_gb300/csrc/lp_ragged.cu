@@ -222,13 +222,7 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     p.stage_offsets = (B + 1u <= kStageOffsetsMax) ? 1u : 0u;
     p.num_sms = (uint32_t)d->sms;
     p.split = 1;
-    {
-        // rows the row-queue kernel holds a ticket (after its 2 queue words) and kMaxSplit
-        // piece slots for
-        const uint32_t by_words = g_max - 2u;
-        const uint32_t by_slots = 2u * g_max / kMaxSplit;
-        p.split_rows = by_words < by_slots ? by_words : by_slots;
-    }
+    p.split_rows = 0;
 
     const uint32_t staged_arrays = (p.loff != p.off) ? 3u : 2u;
     const size_t smem =
@@ -269,6 +263,10 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
         if (S < 1) S = 1;
         if (S > kMaxSplit) S = kMaxSplit;
         p.split = S;
+        // rows the workspace holds a ticket (after the 2 queue words) and S piece slots for
+        const uint32_t by_words = g_max - 2u;
+        const uint32_t by_slots = 2u * g_max / S;
+        p.split_rows = by_words < by_slots ? by_words : by_slots;
     }
     // Launched as a programmatic dependent of the previous kernel on the stream (normally
     // lp_ragged_plan): its CTAs become resident while the plan runs and wait on device.
