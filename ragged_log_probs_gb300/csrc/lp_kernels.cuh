@@ -414,6 +414,35 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
             }
         }
         if constexpr (TOPK && SLOTS == 2) {
+            // K = 63 > 32 lanes: a bound needs 64 distinct elements. With TABW warps on the
+            // row, each lane position takes the two best of the warps' lane maxima (elements
+            // of two different (warp, lane) streams); the 63rd largest of those 64 values
+            // (their second smallest) bounds the top-63. (Tracking a second maximum per lane
+            // in the warp-range kernel costs more than it saves.)
+            if (TABW > 0 && blk != 0 && (blk & (kThrEvery - 1)) == 0) {
+                float hi = neg_inf(), lo = neg_inf();
+                volatile float* tab = lane_tab;
+                tab[w * 32 + lane] = ls.m;
+#pragma unroll
+                for (int j = 0; j < TABW; ++j) {
+                    const float v2 = tab[j * 32 + lane];
+                    lo = fmaxf(lo, fminf(hi, v2));
+                    hi = fmaxf(hi, v2);
+                }
+                // two smallest of the 64 values (lo <= hi in every lane)
+#pragma unroll
+                for (int d2 = 16; d2 > 0; d2 >>= 1) {
+                    const float olo = __shfl_xor_sync(kFull, lo, d2), ohi = __shfl_xor_sync(kFull, hi, d2);
+                    const float nhi = fminf(fmaxf(lo, olo), fminf(hi, ohi));
+                    lo = fminf(lo, olo);
+                    hi = nhi;
+                }
+                sel.thr = fmaxf(sel.thr, hi);
+                if (shared_thr != nullptr) {
+                    if (lane == 0 && sel.thr != neg_inf()) atomicMax(shared_thr, f2ord(sel.thr));
+                    sel.thr = fmaxf(sel.thr, ord2f(*(volatile uint32_t*)shared_thr));
+                }
+            }
             if (blk == 0 && sel.cnt == 0 && sel.thr == neg_inf()) {
                 // Seed the list with each lane's best (and second best) element of this
                 // block, scanned in id order, so the threshold is useful at once.
