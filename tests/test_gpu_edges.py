@@ -253,3 +253,27 @@ def test_split_vocab_pieces_echo_and_variants(split, monkeypatch):
     bv = workloads.with_temperatures(workloads.make_batch("mixed", "cuda", B=6, max_len=9, V=30011,
                                                           variable_extra=2, seed=91), seed=split)
     parity.check_batch(bv, what=f"variable+tau split={split}")
+
+
+@pytest.mark.parametrize("B", [151, 152, 153, 303, 304, 305])
+def test_kernel_choice_boundary(B):
+    # The library's own choice around two rows per SM (152 SMs): split pieces, whole rows,
+    # then warp ranges.
+    b = workloads.make_next_token_batch(B, 20000, levels=3, dist="normal", scale=3.0, device="cuda", seed=B)
+    parity.check_batch(b, rows=parity.sample_rows(B, 40, seed=B), what=f"B={B}")
+
+
+def test_decode_full_size_levels6_sampled():
+    b = workloads.make_batch("decode", "cuda", levels=6)
+    parity.check_batch(b, rows=parity.sample_rows(b.B, 16, seed=6), what="decode levels 6")
+
+
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
+def test_levels6_quantised_ties(kernel, monkeypatch):
+    # The top-63 bound compares with >= against a real element's value: elements equal to
+    # it must still reach the candidates (many exact ties).
+    monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
+    g = torch.Generator().manual_seed(14)
+    x = (torch.round(torch.randn(9, 40000, generator=g) * 4) / 4).cuda()
+    b = workloads.make_custom_batch(x, [1] * 9, [0] * 9, 6, seed=14)
+    parity.check_batch(b, what=f"levels 6 ties/{kernel}")
