@@ -333,7 +333,7 @@ __device__ __forceinline__ float4 load_checked(const float* rowp, const float* v
 // the bound sits much closer to the row's true K-th best than one warp's own.
 template <int SLOTS, bool TOPK, int U, int STAGES, int TABW = 0>
 __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint32_t q0, uint32_t q1, int lane,
-                                             LaneSum& ls, Selector<SLOTS>& sel, bool t_here, uint32_t t,
+                                             LaneSum& ls, Selector<SLOTS>& sel, bool& t_here, uint32_t t,
                                              float& xt, float4* ring, uint32_t* shared_thr = nullptr,
                                              float* lane_tab = nullptr, int w = 0) {
     const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
@@ -345,7 +345,6 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     const uint32_t nblk = qb > qa ? (qb - qa) / (32u * U) : 0u;
     const uint32_t bulk_lo = nblk ? qa : q0;
     const uint32_t bulk_hi = nblk ? qa + nblk * 32u * U : q0;
-    bool xt_pending = t_here;
 
     // ---- bulk: U full vectors per lane per block, no checks --------------------------
     const float* vp = vbase + 4 * (size_t)(qa + lane);
@@ -363,6 +362,11 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
 #pragma unroll
         for (int s0 = 0; s0 < STAGES - 1; ++s0) issue((uint32_t)s0);
     }
+    // Whether this piece holds the target column (t, the column in this row): decided
+    // after the first copies are in flight, so the wait for the token id overlaps them.
+    const int64_t e_lo = 4 * (int64_t)q0 - a, e_hi = 4 * (int64_t)q1 - a;
+    t_here = t < V && (int64_t)t >= e_lo && (int64_t)t < e_hi;
+    bool xt_pending = t_here;
     uint32_t idb = 4u * (qa + (uint32_t)lane) - (uint32_t)a;
     for (uint32_t blk = 0; blk < nblk; ++blk) {
         issue(blk + STAGES - 1);
@@ -810,9 +814,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
             const uint32_t t = d.t;
             const uint32_t t_loc = EXT ? t - p.vocab_base : t;  // column of the target in this shard
             const float* rowp = d.rowp;
-            const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
-            const int64_t e_lo = 4 * (int64_t)q0 - a, e_hi = 4 * (int64_t)q1 - a;
-            const bool t_here = t_loc < V && (int64_t)t_loc >= e_lo && (int64_t)t_loc < e_hi;
+            bool t_here;
 
             LaneSum ls;
             ls.init(d.k);
@@ -993,13 +995,11 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         const uint32_t t = d.t;
         const uint32_t t_loc = EXT ? t - p.vocab_base : t;  // column of the target in this shard
         const float* rowp = d.rowp;
-        const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
         const uint32_t pq0 = (uint32_t)(((uint64_t)p.nq * piece) / S);
         const uint32_t pq1 = (uint32_t)(((uint64_t)p.nq * (piece + 1)) / S);
         const uint32_t wq0 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * w) / NW);
         const uint32_t wq1 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * (w + 1)) / NW);
-        const int64_t e_lo = 4 * (int64_t)wq0 - a, e_hi = 4 * (int64_t)wq1 - a;
-        const bool t_here = t_loc < V && (int64_t)t_loc >= e_lo && (int64_t)t_loc < e_hi;
+        bool t_here;
 
         LaneSum ls;
         ls.init(d.k);
@@ -1008,6 +1008,9 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         float xt = 0.f;
         stream_piece<SLOTS, TOPK, U, STAGES, NW>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr,
                                                  &cm.lane_max[0][0], w);
+        // The CTA's next task is asked for now, so the round trip overlaps the merges.
+        uint32_t next = 0;
+        if (threadIdx.x == 0) next = next_task();
 
         float C = (ls.m == neg_inf()) ? neg_inf() : ls.ref(), Sm = ls.sum();
         warp_lse2_reduce(C, Sm);
@@ -1041,7 +1044,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                 cm.has_xt = 0u;
                 cm.thr = 0u;
                 cm.last = last;
-                cm.row = next_task();  // every thread read cm.row before the merge barriers
+                cm.row = next;  // every thread read cm.row before the merge barriers
             }
         }
         cm.lane_max[w][lane] = neg_inf();  // every warp is past this task's stream
