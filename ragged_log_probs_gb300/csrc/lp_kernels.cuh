@@ -44,10 +44,10 @@ namespace lpk {
 #define LP_STAGES 4  // blocks per warp in the shared-memory ring
 #endif
 #ifndef LP_QUEUE_WARPS
-#define LP_QUEUE_WARPS 8  // warps per CTA of the row-queue kernel
+#define LP_QUEUE_WARPS 12  // warps per CTA of the row-queue kernel
 #endif
 #ifndef LP_QUEUE_STAGES
-#define LP_QUEUE_STAGES 4  // ring depth of the row-queue kernel
+#define LP_QUEUE_STAGES 3  // ring depth of the row-queue kernel
 #endif
 #ifndef LP_QUEUE_UNROLL
 #define LP_QUEUE_UNROLL 4  // vectors per lane per block in the row-queue kernel
