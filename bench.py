@@ -81,11 +81,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def queue_rows_limit() -> int:
-    """The library runs the row-queue kernel when at most this many rows can come out
-    (two per SM: 304 on GB300), else the warp-range kernel."""
+def uses_row_queue(rows_bound: int, V: int) -> bool:
+    """The library's kernel choice: the row-queue kernel when at most two rows per SM can
+    come out, or at most five of at most 64K logits; else the warp-range kernel."""
     import torch
-    return 2 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return rows_bound <= 2 * sms or (rows_bound <= 5 * sms and V <= 65536)
 
 
 def algorithmic_bytes(R: int, V: int, W: int, B: int) -> int:
@@ -448,7 +449,8 @@ def run_ours(args, rank: int, world: int, dist):
     if rec and rec.get("source_hash") == kernel_source_hash():
         traffic = rec["bytes_per_launch"]
     entry = "lp_ragged_shard_partials" if sharded else ("lp_ragged_compute_ex" if extended else "lp_ragged_compute")
-    kernel_name = (f"k_rows_cta ({entry}, row queue)" if min(T, T_logits) <= queue_rows_limit()
+    shard_V = full_logits.shape[1]
+    kernel_name = (f"k_rows_cta ({entry}, row queue)" if uses_row_queue(min(T, T_logits), shard_V)
                    else f"k_rows ({entry}, warp ranges)")
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                 "timing": f"CUDA events around one CUDA-graph replay of {n_ev} back-to-back compute launches, same "

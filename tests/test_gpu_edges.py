@@ -255,12 +255,13 @@ def test_split_vocab_pieces_echo_and_variants(split, monkeypatch):
     parity.check_batch(bv, what=f"variable+tau split={split}")
 
 
-@pytest.mark.parametrize("B", [151, 152, 153, 303, 304, 305])
-def test_kernel_choice_boundary(B):
-    # The library's own choice around two rows per SM (152 SMs): split pieces, whole rows,
-    # then warp ranges.
-    b = workloads.make_next_token_batch(B, 20000, levels=3, dist="normal", scale=3.0, device="cuda", seed=B)
-    parity.check_batch(b, rows=parity.sample_rows(B, 40, seed=B), what=f"B={B}")
+@pytest.mark.parametrize("B,V", [(151, 20000), (152, 20000), (153, 20000), (304, 20000), (305, 20000),
+                                 (760, 20000), (761, 20000), (304, 70000), (305, 70000)])
+def test_kernel_choice_boundary(B, V):
+    # The library's own choice (152 SMs): split pieces below one row per SM, whole rows up
+    # to two per SM (five when rows hold at most 64K logits), then warp ranges.
+    b = workloads.make_next_token_batch(B, V, levels=3, dist="normal", scale=3.0, device="cuda", seed=B)
+    parity.check_batch(b, rows=parity.sample_rows(B, 40, seed=B), what=f"B={B} V={V}")
 
 
 def test_decode_full_size_levels6_sampled():
