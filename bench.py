@@ -82,11 +82,11 @@ def kernel_source_hash() -> str:
 
 
 def uses_row_queue(rows_bound: int, V: int) -> bool:
-    """The library's kernel choice: the row-queue kernel when at most two rows per SM can
-    come out, or at most five of at most 64K logits; else the warp-range kernel."""
+    """The library's kernel choice: the row-queue kernel when at most three rows per SM
+    can come out, or at most five of at most 40K logits; else the warp-range kernel."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return rows_bound <= 2 * sms or (rows_bound <= 5 * sms and V <= 65536)
+    return rows_bound <= 3 * sms or (rows_bound <= 5 * sms and V <= 40960)
 
 
 def algorithmic_bytes(R: int, V: int, W: int, B: int) -> int:

@@ -38,10 +38,10 @@ namespace lpk {
 #define LP_UNROLL 4
 #endif
 #ifndef LP_MIN_BLOCKS
-#define LP_MIN_BLOCKS 3
+#define LP_MIN_BLOCKS 2
 #endif
 #ifndef LP_STAGES
-#define LP_STAGES 4  // blocks per warp in the shared-memory ring
+#define LP_STAGES 5  // blocks per warp in the shared-memory ring
 #endif
 #ifndef LP_QUEUE_WARPS
 #define LP_QUEUE_WARPS 12  // warps per CTA of the row-queue kernel
