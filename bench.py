@@ -66,9 +66,9 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 135173120, "source_hash": "d494a3c2f2d6de1f",
+    "decode": {"bytes_per_launch": 134999040, "source_hash": "58e634fa34920627",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 904192768, "source_hash": "d494a3c2f2d6de1f",
+    "prefill": {"bytes_per_launch": 903291136, "source_hash": "58e634fa34920627",
                 "capture": "profiles/k_rows_prefill.md"},
 }
 
