@@ -66,18 +66,44 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 134999040, "source_hash": "58e634fa34920627",
+    "decode": {"bytes_per_launch": 134999040, "source_hash": "cb768fcaba10c317",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 903291136, "source_hash": "58e634fa34920627",
+    "prefill": {"bytes_per_launch": 903291136, "source_hash": "cb768fcaba10c317",
                 "capture": "profiles/k_rows_prefill.md"},
 }
+
+
+def _code_only(text: str) -> str:
+    """The source with // comments and trailing blanks removed (string literals kept), so
+    that a comment edit does not void counters taken on the same code."""
+    out = []
+    for line in text.splitlines():
+        in_str, esc, cut = False, False, len(line)
+        for i, ch in enumerate(line):
+            if in_str:
+                if esc:
+                    esc = False
+                elif ch == "\\":
+                    esc = True
+                elif ch == '"':
+                    in_str = False
+            elif ch == '"':
+                in_str = True
+            elif ch == "/" and line[i + 1:i + 2] == "/":
+                cut = i
+                break
+        code = line[:cut].rstrip()
+        if code:
+            out.append(code)
+    return "\n".join(out)
 
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "ragged_log_probs_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

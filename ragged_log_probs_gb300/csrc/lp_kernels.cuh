@@ -861,18 +861,18 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
 }
 
 // ---------------------------------------------------------------------------------
-// Few rows (at most two per SM, e.g. next-token logits for a decode batch): CTAs of NW
-// warps take tasks from a queue (atomic counters); a task is a whole row, or, when there
-// are fewer rows than twice the SMs, one of S contiguous pieces of a row (split-vocab:
-// S = min(2*SMs / rows, row length / 16 KB, 64), chosen on the host). The CTA's warps
-// split the task into NW contiguous parts and merge their results in shared memory; a
-// whole row is written at once, a piece is published to the workspace and the CTA that
-// takes the row's last ticket merges the S pieces with all its warps (each warp merges
-// every NW-th piece, then the shared-memory tree). At most ceil(tasks / SMs) CTAs of an
-// SM take part (a per-SM slot counter), so all tasks stream at once and no SM carries
-// more than its share. The warps of a CTA share their lanes' running maxima for the
-// top-k threshold (see stream_piece). The last CTA to leave resets the queue words and
-// the per-SM counters for the next call; the merging CTA resets its row's ticket.
+// Few rows (up to three per SM, or five when rows are at most 40K logits; e.g. next-token
+// logits for a decode batch): CTAs of NW warps take tasks; a task is a whole row, or, when
+// there are fewer rows than twice the SMs, one of S contiguous pieces of a row
+// (split-vocab: S = min(2*SMs / rows, row length / 16 KB, 64), chosen on the host). The
+// CTA's warps split the task into NW contiguous parts and merge their results in shared
+// memory; a whole row is written at once, a piece is published to the workspace and the
+// CTA that takes the row's last ticket merges the S pieces with all its warps (each warp
+// merges every NW-th piece, then the shared-memory tree). The first CTA on each SM starts
+// on a task of its own without an atomic, every later task comes from one queue counter,
+// so all SMs stream from the start. The warps of a CTA share their lanes' running maxima
+// for the top-k threshold (see stream_piece). The last CTA to leave resets the queue
+// words for the next call; the merging CTA resets its row's ticket.
 template <int NW>
 struct CtaMerge {
     float list_x[NW][64];

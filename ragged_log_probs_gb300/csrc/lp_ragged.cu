@@ -254,7 +254,7 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
         occ = occupancy(d, v, launch_smem);
         if (occ == 0) return LP_ERR_CUDA;
         grid = (uint32_t)d->sms * (uint32_t)occ;
-        // split-vocab for small batches: pieces per row so that the tasks fill two per SM
+        // split-vocab for small batches: pieces per row so that the tasks number about two per SM
         uint32_t S = (2u * (uint32_t)d->sms) / (r_max ? r_max : 1u);
         const uint32_t by_len = p.nq / kMinSplitVec;
         if (S > by_len) S = by_len;
