@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 
 namespace lpk {
 
@@ -37,6 +38,37 @@ __device__ __forceinline__ float4 ldg_stream(const float* p) {
 __device__ __forceinline__ void cp_async16(uint32_t smem_addr, const float* gptr) {
     asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(smem_addr), "l"(gptr) : "memory");
 }
+// U such copies of one lane: dst + 512*u <- src + 512*u bytes (a warp's 32 lanes fill
+// 512 contiguous bytes per u), with the offsets as immediates of the instructions.
+template <int OFF>
+__device__ __forceinline__ void cp_async16_at(uint32_t dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0+%2], [%1+%2], 16;" ::"r"(dst), "l"(src), "n"(OFF)
+                 : "memory");
+}
+template <int... I>
+__device__ __forceinline__ void cp_async16_seq(uint32_t dst, const float* src, std::integer_sequence<int, I...>) {
+    (cp_async16_at<512 * I>(dst, src), ...);
+}
+template <int U>
+__device__ __forceinline__ void cp_async16_run(uint32_t dst, const float* src) {
+    cp_async16_seq(dst, src, std::make_integer_sequence<int, U>{});
+}
+// The same for a partial block: copies u with 32*u < n (n: the block's vectors left from
+// this lane); the other slots get four -inf (a plain shared store, seen by this lane's
+// later loads in program order).
+__device__ __forceinline__ void sts_neg_inf4(uint32_t dst) {
+    const uint32_t ni = 0xff800000u;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(ni) : "memory");
+}
+template <int... I>
+__device__ __forceinline__ void cp_async16_seq_pad(uint32_t dst, const float* src, int n,
+                                                   std::integer_sequence<int, I...>) {
+    ((32 * I < n ? cp_async16_at<512 * I>(dst, src) : sts_neg_inf4(dst + 512 * I)), ...);
+}
+template <int U>
+__device__ __forceinline__ void cp_async16_run_pad(uint32_t dst, const float* src, int n) {
+    cp_async16_seq_pad(dst, src, n, std::make_integer_sequence<int, U>{});
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -65,6 +97,12 @@ __device__ __forceinline__ float ord2f(uint32_t o) {
 
 __device__ __forceinline__ float pick(const float4& v, int k) {
     return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+// Element mask of the vector whose first id is id0: the elements with id < end.
+__device__ __forceinline__ uint32_t ids_below(uint32_t id0, uint32_t end) {
+    const int n = (int)(end - id0);
+    return n >= 4 ? 0xFu : (n <= 0 ? 0u : (1u << n) - 1u);
 }
 
 __device__ __forceinline__ uint32_t ge_mask(const float4& v, float thr) {

@@ -185,28 +185,40 @@ __device__ __forceinline__ uint64_t sk_owner(uint64_t v, uint64_t Q, uint64_t G)
     return ((v + 1) * G - 1) / Q;
 }
 
-// Per-lane running sum in the log2 domain.
+// Per-lane running sum in the log2 domain: s = sum of 2^(x*k - c) over the logits seen,
+// with a reference c that moves lazily. It is set by the first finite block and moved
+// up only when a block's maximum exceeds it by more than kHeadroom (so every term stays
+// below 2^kHeadroom and the sum far from overflow); any reference gives the same
+// logsumexp, c + log2(s). m, the lane's true running maximum, feeds the top-k bound.
+constexpr float kHeadroom = 8.f;
+constexpr float kNoRef = 3.402823466e38f;  // nc before the first finite logit
 struct LaneSum {
     float m;   // largest logit seen (-inf: none)
-    float nc;  // minus the reference c = m * k rounded (0 while m is -inf)
+    float nc;  // minus the reference c (kNoRef while m is -inf)
     float2 s;  // sum of 2^(x * k - c), in two halves (packed adds)
     float k;   // log2(e) / temperature
     __device__ __forceinline__ void init(float scale) {
         m = neg_inf();
-        nc = 0.f;
+        nc = kNoRef;
         s = make_float2(0.f, 0.f);
         k = scale;
     }
     __device__ __forceinline__ float ref() const { return -nc; }
     __device__ __forceinline__ float sum() const { return s.x + s.y; }
-    __device__ __forceinline__ void raise(float nm) {
+    // Account for a block whose largest logit is bm, before its terms are added.
+    // Without a reference, bm*k + kNoRef is above the headroom for every finite bm
+    // (and -inf for an all -inf block, whose terms are then 2^-inf = 0).
+    __device__ __forceinline__ void note(float bm) {
+        m = fmaxf(m, bm);
+        if (fmaf(bm, k, nc) > kHeadroom) rebase(bm);
+    }
+    __device__ __forceinline__ void rebase(float nm) {
         const float c_new = nm * k;
         if (s.x != 0.f || s.y != 0.f) {
             const float f = ex2(-nc - c_new);
             s = ffma2(s, make_float2(f, f), make_float2(0.f, 0.f));
         }
         nc = -c_new;
-        m = nm;
     }
     // Add the terms of four logits: two packed FMAs, four EX2, two packed adds.
     __device__ __forceinline__ void add4(const float4& v) {
@@ -341,26 +353,37 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     const uint32_t qf = a ? 1u : 0u;
     const uint32_t qe = (V + (uint32_t)a) >> 2;
     const uint32_t nfull = qe > qf ? qe - qf : 0u;
-    const uint32_t qa = max(q0, qf), qb = min(q1, qe);
-    const uint32_t nblk = qb > qa ? (qb - qa) / (32u * U) : 0u;
-    const uint32_t bulk_lo = nblk ? qa : q0;
-    const uint32_t bulk_hi = nblk ? qa + nblk * 32u * U : q0;
+    // [qa, qb): the piece's whole 16-byte vectors, streamed through the ring; before and
+    // after them at most the row's partial first and last vectors (unaligned rows only).
+    const uint32_t qa = max(q0, qf);
+    const uint32_t qb = max(min(q1, qe), qa);
+    const uint32_t nblk = (qb - qa + 32u * U - 1u) / (32u * U);
+    const uint32_t rem = (qb - qa) % (32u * U);  // vectors in the last block when it is partial
 
-    // ---- bulk: U full vectors per lane per block, no checks --------------------------
-    const float* vp = vbase + 4 * (size_t)(qa + lane);
+    // ---- bulk: U vectors per lane per block ---------------------------------------------
+    // The issue side walks the source and the ring slots by running offsets (no index
+    // arithmetic per block); the U copies of a block use immediate address offsets. In a
+    // partial last block a lane copies only its vectors below qb and fills the others'
+    // ring slots with -inf (no term, no maximum; the top-k keeps ids below id_end), so
+    // the piece's tail streams through the ring like the rest.
+    constexpr uint32_t kStage = U * 512u;  // ring bytes per block and warp
+    const float* src = vbase + 4 * (size_t)(qa + lane);
     const uint32_t ring_lane = (uint32_t)__cvta_generic_to_shared(ring + lane);
-    auto issue = [&](uint32_t blk) {
-        if (blk < nblk) {
-            const float* src = vp + (size_t)blk * 128u * U;
-            const uint32_t dst = ring_lane + (blk % STAGES) * (U * 512u);
-#pragma unroll
-            for (int u = 0; u < U; ++u) cp_async16(dst + 512u * u, src + 128 * u);
+    uint32_t put = 0, get = 0;  // ring offsets of the next block to issue / to reduce
+    uint32_t unissued = nblk;
+    auto issue = [&]() {
+        if (unissued) {
+            if (unissued == 1u && rem != 0u) cp_async16_run_pad<U>(ring_lane + put, src, (int)rem - lane);
+            else cp_async16_run<U>(ring_lane + put, src);
+            src += 128 * U;
+            put = put == (STAGES - 1) * kStage ? 0u : put + kStage;
+            --unissued;
         }
         cp_async_commit();
     };
     if (nblk) {
 #pragma unroll
-        for (int s0 = 0; s0 < STAGES - 1; ++s0) issue((uint32_t)s0);
+        for (int s0 = 0; s0 < STAGES - 1; ++s0) issue();
     }
     // Whether this piece holds the target column (t, the column in this row): decided
     // after the first copies are in flight, so the wait for the token id overlaps them.
@@ -368,11 +391,13 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     t_here = t < V && (int64_t)t >= e_lo && (int64_t)t < e_hi;
     bool xt_pending = t_here;
     uint32_t idb = 4u * (qa + (uint32_t)lane) - (uint32_t)a;
+    const uint32_t id_end = 4u * qb - (uint32_t)a;  // ids of the ring's padding start here
     for (uint32_t blk = 0; blk < nblk; ++blk) {
-        issue(blk + STAGES - 1);
+        issue();
         cp_async_wait<STAGES - 1>();
         float4 v[U];
-        const float4* stage = ring + (blk % STAGES) * (U * 32u) + lane;
+        const float4* stage = ring + lane + get / 16u;
+        get = get == (STAGES - 1) * kStage ? 0u : get + kStage;
 #pragma unroll
         for (int u = 0; u < U; ++u) v[u] = stage[32 * u];
         if (xt_pending) {  // the target id has arrived by now
@@ -386,7 +411,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
 #pragma unroll
         for (int u = 1; u + 1 < U; u += 2) bm = max3(bm, mu[u], mu[u + 1]);
         if ((U & 1) == 0) bm = fmaxf(bm, mu[U - 1]);
-        if (bm > ls.m) ls.raise(bm);
+        ls.note(bm);
 #pragma unroll
         for (int u = 0; u < U; ++u) ls.add4(v[u]);
 
@@ -413,7 +438,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     if (__any_sync(kFull, mu[u] >= sel.thr))
-                        sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr), lane);
+                        sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr) & ids_below(idb + 128u * u, id_end), lane);
                 }
             }
         }
@@ -478,30 +503,33 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
                         uint32_t ex = 0;  // the seeded elements are already in the list
                         if ((p1 >> 2) == u) ex |= 1u << (p1 & 3);
                         if (SLOTS == 2 && (p2 >> 2) == u) ex |= 1u << (p2 & 3);
-                        sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr) & ~ex, lane);
+                        sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr) & ~ex & ids_below(idb + 128u * u, id_end),
+                                   lane);
                     }
                 }
             } else if (__any_sync(kFull, bm >= sel.thr)) {
 #pragma unroll
-                for (int u = 0; u < U; ++u) sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr), lane);
+                for (int u = 0; u < U; ++u)
+                    sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr) & ids_below(idb + 128u * u, id_end), lane);
             }
         }
         idb += 128u * U;
     }
     if (xt_pending && lane == 0) xt = rowp[t];
 
-    // ---- edges: the partial first/last vectors and the tail, one checked vector per lane
+    // ---- edges: the row's partial first and last vectors (rows that do not start or end
+    // on a 16-byte boundary), one checked vector per lane
 #pragma unroll 1
     for (int part = 0; part < 2; ++part) {
-        const uint32_t lo = part ? bulk_hi : q0;
-        const uint32_t hi = part ? q1 : bulk_lo;
+        const uint32_t lo = part ? qb : q0;
+        const uint32_t hi = part ? q1 : min(qa, q1);
         for (uint32_t qs = lo; qs < hi; qs += 32) {
             const uint32_t q = qs + (uint32_t)lane;
             float4 v = make_float4(neg_inf(), neg_inf(), neg_inf(), neg_inf());
             uint32_t vm = 0;
             if (q < hi) v = load_checked(rowp, vbase, q, a, V, qf, nfull, vm);
             const float mx = max4(v);
-            if (mx > ls.m) ls.raise(mx);
+            ls.note(mx);
             ls.add4(v);
             if constexpr (TOPK) {
                 if (__any_sync(kFull, mx >= sel.thr))
@@ -512,6 +540,9 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     if constexpr (TOPK) {
         if (sel.cnt > 0) sel.flush(lane);
     }
+    // Leave the reference at the lane's maximum (c = m * k), the form the merges and the
+    // row tuples use.
+    if (ls.m != neg_inf()) ls.rebase(ls.m);
 }
 
 // Write one finished row: K top columns and the target column. (C, S) are the row's
