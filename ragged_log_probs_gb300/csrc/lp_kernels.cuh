@@ -292,6 +292,28 @@ struct Selector {
         cnt = cnt > 32 ? cnt - 32 : 0;
         thr = fmaxf(thr, L.kth(K));
     }
+    // Append the elements of one ring block flagged in mk: bit 4u+k is element k of the
+    // lane's vector u, whose value sits at slot_f[128u + 4 lane + k] and whose id is
+    // idb + 128u + k. Warp-uniform call, one ballot round per element a lane appends
+    // (usually one). An element stays flagged if a flush raises the threshold meanwhile:
+    // below the threshold it is only extra work for the next merge.
+    __device__ __forceinline__ void append_block(const float* slot_f, uint32_t mk, uint32_t idb, int lane) {
+        const uint32_t lt = (1u << lane) - 1u;
+        unsigned any = __ballot_sync(kFull, mk != 0);
+        while (any) {
+            if (mk) {
+                const uint32_t e = (uint32_t)(__ffs(mk) - 1);
+                mk &= mk - 1;
+                const uint32_t off = 128u * (e >> 2) + (e & 3u);
+                const int slot = cnt + __popc(any & lt);
+                cx[slot] = slot_f[off + 4u * (uint32_t)lane];
+                ci[slot] = idb + off;
+            }
+            cnt += __popc(any);
+            if (cnt >= 32) flush(lane);
+            any = __ballot_sync(kFull, mk != 0);
+        }
+    }
     // Append the elements of v flagged in pm (bit k: element k, id id0 + k).
     // Warp-uniform call; the threshold may rise while appending.
     __device__ __forceinline__ void append(const float4& v, uint32_t id0, uint32_t pm, int lane) {
@@ -330,6 +352,29 @@ __device__ __forceinline__ float4 load_checked(const float* rowp, const float* v
         if (e >= 0 && e < (int64_t)V) { t[k] = rowp[e]; vm |= 1u << k; }
     }
     return make_float4(t[0], t[1], t[2], t[3]);
+}
+
+// Threshold refreshes: blocks 0, 1, 2, 4, then every kThrEvery blocks.
+__device__ __forceinline__ bool refresh_due(uint32_t blk) {
+    return (blk & (kThrEvery - 1)) == 0 || (blk < kThrEvery && (blk & (blk - 1)) == 0);
+}
+
+// Candidate mask of one block: bit 4u+k set when element k of vector u is >= thr.
+template <int U>
+__device__ __forceinline__ uint32_t block_mask(const float4 (&v)[U], float thr) {
+    uint32_t mk = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) mk |= ge_mask(v[u], thr) << (4 * u);
+    return mk;
+}
+// Elements of a block that are not ring padding (ids below id_end): all but in a piece's
+// partial last block.
+template <int U>
+__device__ __forceinline__ uint32_t live_mask(uint32_t idb, uint32_t id_end) {
+    uint32_t mk = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) mk |= ids_below(idb + 128u * u, id_end) << (4 * u);
+    return mk;
 }
 
 // Stream vectors [q0, q1) of one row: running sum per lane, top-k per warp.
@@ -397,6 +442,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
         cp_async_wait<STAGES - 1>();
         float4 v[U];
         const float4* stage = ring + lane + get / 16u;
+        const float* slot_f = reinterpret_cast<const float*>(ring + get / 16u);  // the block, all lanes
         get = get == (STAGES - 1) * kStage ? 0u : get + kStage;
 #pragma unroll
         for (int u = 0; u < U; ++u) v[u] = stage[32 * u];
@@ -419,8 +465,9 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
             // The K-th largest of the 32 lanes' running maxima is the value of K distinct
             // elements already seen, so no element below it can be in the top-k: a
             // threshold that follows the warp's true K-th best at the cost of one float
-            // sort, refreshed on the first block and then every kThrEvery blocks.
-            if ((blk & (kThrEvery - 1)) == 0) {
+            // sort, refreshed on blocks 0, 1, 2 and 4 (it rises fastest early) and then
+            // every kThrEvery blocks.
+            if (refresh_due(blk)) {
                 float lm = ls.m;
                 if constexpr (TABW > 0) {
                     volatile float* tab = lane_tab;
@@ -435,11 +482,9 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
                 }
             }
             if (__any_sync(kFull, bm >= sel.thr)) {
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (__any_sync(kFull, mu[u] >= sel.thr))
-                        sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr) & ids_below(idb + 128u * u, id_end), lane);
-                }
+                uint32_t mk = block_mask<U>(v, sel.thr);
+                if (blk + 1u == nblk && rem != 0u) mk &= live_mask<U>(idb, id_end);
+                sel.append_block(slot_f, mk, idb, lane);
             }
         }
         if constexpr (TOPK && SLOTS == 2) {
@@ -448,7 +493,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
             // of two different (warp, lane) streams); the 63rd largest of those 64 values
             // (their second smallest) bounds the top-63. (Tracking a second maximum per lane
             // in the warp-range kernel costs more than it saves.)
-            if (TABW > 0 && blk != 0 && (blk & (kThrEvery - 1)) == 0) {
+            if (TABW > 0 && blk != 0 && refresh_due(blk)) {
                 float hi = neg_inf(), lo = neg_inf();
                 volatile float* tab = lane_tab;
                 tab[w * 32 + lane] = ls.m;
@@ -498,19 +543,17 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
                 }
                 sel.thr = sel.L.kth(sel.K);
                 if (__any_sync(kFull, bm >= sel.thr)) {
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        uint32_t ex = 0;  // the seeded elements are already in the list
-                        if ((p1 >> 2) == u) ex |= 1u << (p1 & 3);
-                        if (SLOTS == 2 && (p2 >> 2) == u) ex |= 1u << (p2 & 3);
-                        sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr) & ~ex & ids_below(idb + 128u * u, id_end),
-                                   lane);
-                    }
+                    uint32_t ex = 0;  // the seeded elements are already in the list
+                    if (p1 >= 0) ex |= 1u << p1;
+                    if (SLOTS == 2 && p2 >= 0) ex |= 1u << p2;
+                    uint32_t mk = block_mask<U>(v, sel.thr) & ~ex;
+                    if (blk + 1u == nblk && rem != 0u) mk &= live_mask<U>(idb, id_end);
+                    sel.append_block(slot_f, mk, idb, lane);
                 }
             } else if (__any_sync(kFull, bm >= sel.thr)) {
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    sel.append(v[u], idb + 128u * u, ge_mask(v[u], sel.thr) & ids_below(idb + 128u * u, id_end), lane);
+                uint32_t mk = block_mask<U>(v, sel.thr);
+                if (blk + 1u == nblk && rem != 0u) mk &= live_mask<U>(idb, id_end);
+                sel.append_block(slot_f, mk, idb, lane);
             }
         }
         idb += 128u * U;
