@@ -319,11 +319,15 @@ def run_ours(args, rank: int, world: int, dist):
 
     def step(i, st=None):
         st = stream if st is None else st
-        lp.plan(pos_off, batch.echo, T, ws, output_row_offsets=out_off, stream=st)
-        launch_compute(copies[i % n_copies], batch.logit_row_offsets, batch.input_row_offsets, batch.tokens,
-                       batch.sampled_tokens, batch.echo, batch.temperatures, st)
         if sharded:
+            lp.plan(pos_off, batch.echo, T, ws, output_row_offsets=out_off, stream=st)
+            launch_compute(copies[i % n_copies], batch.logit_row_offsets, batch.input_row_offsets, batch.tokens,
+                           batch.sampled_tokens, batch.echo, batch.temperatures, st)
             lp.shard_merge(gathered, SHARDS, R, V, out_off, levels, out_lp, out_tok, ws, stream=st)
+        else:  # plan + reduction in one call (lp_ragged_step)
+            lp.step(copies[i % n_copies], batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, batch.echo,
+                    levels, out_off, out_lp, out_tok, ws, input_row_offsets=batch.input_row_offsets,
+                    temperatures=batch.temperatures, stream=st)
 
     def capture(n, body):
         """n calls of body(k, stream) captured in one CUDA graph (launch-bound loops replay
@@ -430,11 +434,14 @@ def run_ours(args, rank: int, world: int, dist):
             d_logits.copy_(h_logits, non_blocking=True)
             for d, h in zip(d_ints, h_ints):
                 d.copy_(h, non_blocking=True)
-            lp.plan(d_ioff if d_ioff is not None else d_ints[0], d_ints[3], T, ws, output_row_offsets=out_off,
-                    stream=stream)
-            launch_compute(d_logits, d_ints[0], d_ioff, d_ints[1], d_ints[2], d_ints[3], d_tau)
             if sharded:
+                lp.plan(d_ioff if d_ioff is not None else d_ints[0], d_ints[3], T, ws, output_row_offsets=out_off,
+                        stream=stream)
+                launch_compute(d_logits, d_ints[0], d_ioff, d_ints[1], d_ints[2], d_ints[3], d_tau)
                 lp.shard_merge(gathered, SHARDS, R, V, out_off, levels, out_lp, out_tok, ws, stream=stream)
+            else:
+                lp.step(d_logits, d_ints[0], d_ints[1], d_ints[2], d_ints[3], levels, out_off, out_lp, out_tok, ws,
+                        input_row_offsets=d_ioff, temperatures=d_tau, stream=stream)
             h_lp.copy_(out_lp, non_blocking=True)
             h_tok.copy_(out_tok, non_blocking=True)
 

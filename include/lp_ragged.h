@@ -159,6 +159,33 @@ lp_status lp_ragged_compute_ex(const float *logits, uint32_t T_logits, uint32_t 
                                lp_stream_t stream);
 
 /*
+ * Steps 1 and 2 in one call, for a serving step whose output buffers are sized ahead
+ * (R <= T always): lp_ragged_plan on the positions offsets (input_row_offsets, or
+ * logit_row_offsets when it is NULL), then the reduction of lp_ragged_compute_ex, both
+ * enqueued on `stream` by the library. Because the reduction directly follows the plan,
+ * it streams the logits while the plan is still running (it derives the output rows
+ * from the offsets itself, with the plan's checks) and waits for the plan only before
+ * it touches the workspace counters or the status word; the rows are identical to
+ * lp_ragged_plan + lp_ragged_compute_ex.
+ *   output_row_offsets   device out, uint32[B+1] (as lp_ragged_plan)
+ *   host_rows_and_status pinned host out, uint32[2] or NULL: {R, status}, copied after
+ *                        the reduction (so the status holds the plan's and the
+ *                        reduction's bits); valid once the stream reaches that point
+ *   out_logprobs         device out, float[out_rows][W]
+ *   out_tokens           device out, uint32[out_rows][W]
+ *   out_rows             rows the outputs hold, > 0; when R > out_rows nothing is
+ *                        written and the LP_ERR_OFFSETS bit is set
+ * Other arguments, workspace and checks: as lp_ragged_plan and lp_ragged_compute_ex.
+ * Errors: those of both calls.
+ */
+lp_status lp_ragged_step(const float *logits, uint32_t T_logits, uint32_t V, const uint32_t *logit_row_offsets,
+                         const uint32_t *input_row_offsets, uint32_t T, uint32_t B, const uint32_t *tokens,
+                         const uint32_t *sampled_tokens, const uint8_t *echo, const float *temperatures,
+                         uint32_t levels, uint32_t *output_row_offsets, uint32_t *host_rows_and_status,
+                         float *out_logprobs, uint32_t *out_tokens, uint32_t out_rows, void *workspace,
+                         size_t workspace_bytes, lp_stream_t stream);
+
+/*
  * Vocab-parallel form (the forward pass runs on tensor-parallel workers, SGLang page
  * "logprob、finish reason 与 output processing", section "第一步：ModelRunner.forward()
  * 输出 logits"; with the lm_head split by vocabulary each rank holds a contiguous range

@@ -33,7 +33,7 @@ STATUS_NAMES = {
     5: "LP_ERR_TOKEN_RANGE", 6: "LP_ERR_WORKSPACE", 7: "LP_ERR_CUDA", 8: "LP_ERR_TEMPERATURE",
 }
 EXPORTS = ("lp_ragged_workspace_size", "lp_ragged_plan", "lp_ragged_compute", "lp_ragged_compute_ex",
-           "lp_ragged_tuple_bytes", "lp_ragged_shard_partials", "lp_ragged_shard_merge",
+           "lp_ragged_step", "lp_ragged_tuple_bytes", "lp_ragged_shard_partials", "lp_ragged_shard_merge",
            "lp_ragged_read_status", "lp_ragged_strerror")
 
 
@@ -68,6 +68,9 @@ def load() -> ctypes.CDLL:
     lib.lp_ragged_compute.restype = ctypes.c_int
     lib.lp_ragged_compute_ex.argtypes = [vp, u32, u32, vp, vp, u32, u32, vp, vp, vp, vp, vp, u32, vp, vp, vp, sz, vp]
     lib.lp_ragged_compute_ex.restype = ctypes.c_int
+    lib.lp_ragged_step.argtypes = [vp, u32, u32, vp, vp, u32, u32, vp, vp, vp, vp, u32, vp, vp, vp, vp, u32, vp, sz,
+                                   vp]
+    lib.lp_ragged_step.restype = ctypes.c_int
     lib.lp_ragged_tuple_bytes.argtypes = [u32]
     lib.lp_ragged_tuple_bytes.restype = u32
     lib.lp_ragged_shard_partials.argtypes = [vp, u32, u32, u32, vp, vp, u32, u32, vp, vp, vp, vp, vp, u32, vp, u32,
@@ -222,6 +225,54 @@ def compute_ex(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: to
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc:
         raise LpError(rc, "lp_ragged_compute_ex")
+
+
+def step(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: torch.Tensor, sampled_tokens: torch.Tensor,
+         echo: torch.Tensor, levels: int, output_row_offsets: torch.Tensor, out_logprobs: torch.Tensor,
+         out_tokens: torch.Tensor, workspace: torch.Tensor, input_row_offsets: Optional[torch.Tensor] = None,
+         temperatures: Optional[torch.Tensor] = None, host_out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Enqueue ``lp_ragged_step``: plan and reduction in one call, the reduction streaming
+    while the plan runs. ``out_logprobs`` / ``out_tokens`` are [rows, W] with rows >= R
+    (R <= T); ``host_out`` (pinned int32 [2]) receives {R, status of plan and reduction}."""
+    lib = load()
+    if logits.dim() != 2 or logits.dtype != torch.float32 or not logits.is_cuda:
+        raise TypeError("logits must be a 2-D float32 CUDA tensor")
+    if logits.stride(1) != 1 or logits.stride(0) != logits.shape[1]:
+        raise ValueError("logits must be row-major contiguous")
+    T_logits, V = logits.shape
+    B = logit_row_offsets.numel() - 1
+    T = tokens.numel()
+    ioff = 0
+    if input_row_offsets is not None:
+        ioff = _dev_u32(input_row_offsets, "input_row_offsets", B + 1)
+    elif T != T_logits:
+        raise ValueError("without input_row_offsets every position needs a logits row (tokens and logits rows)")
+    tp = 0
+    if temperatures is not None:
+        if temperatures.dtype != torch.float32 or not temperatures.is_cuda or not temperatures.is_contiguous() \
+                or temperatures.numel() < B:
+            raise TypeError("temperatures must be a contiguous float32 CUDA tensor with B entries")
+        tp = temperatures.data_ptr()
+    W = out_per_token(levels)
+    if out_logprobs.dtype != torch.float32 or not out_logprobs.is_cuda or not out_logprobs.is_contiguous() \
+            or out_logprobs.dim() != 2 or out_logprobs.shape[1] != W:
+        raise TypeError(f"out_logprobs must be a contiguous float32 CUDA tensor [rows, {W}]")
+    rows = out_logprobs.shape[0]
+    if out_tokens.shape != out_logprobs.shape:
+        raise ValueError("out_tokens must have the shape of out_logprobs")
+    hp = 0
+    if host_out is not None:
+        if host_out.dtype != torch.int32 or host_out.numel() < 2 or host_out.is_cuda or not host_out.is_pinned():
+            raise TypeError("host_out must be a pinned int32 CPU tensor with 2 elements")
+        hp = host_out.data_ptr()
+    rc = lib.lp_ragged_step(
+        logits.data_ptr(), T_logits, V, _dev_u32(logit_row_offsets, "logit_row_offsets", B + 1), ioff, T, B,
+        _dev_u32(tokens, "tokens", T), _dev_u32(sampled_tokens, "sampled_tokens", B), _dev_u8(echo, "echo", B), tp,
+        levels, _dev_u32(output_row_offsets, "output_row_offsets", B + 1), hp, out_logprobs.data_ptr(),
+        _dev_u32(out_tokens, "out_tokens"), rows, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc:
+        raise LpError(rc, "lp_ragged_step")
 
 
 def tuple_bytes(levels: int) -> int:

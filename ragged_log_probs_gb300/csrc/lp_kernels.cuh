@@ -111,6 +111,12 @@ struct RowsParams {
     uint32_t tuple_rows;     // vocab shard mode: rows the tuple buffer holds
     uint32_t split;          // row-queue kernel: pieces per row (1: whole rows)
     uint32_t split_rows;     // row-queue kernel: rows the workspace holds tickets and pieces for
+    // Launched by lp_ragged_step directly after its lp_ragged_plan (which ran after all
+    // earlier work): with staged offsets the row kernel derives the output rows itself and
+    // streams before the plan has finished, waiting for it only before it touches the
+    // counters or the status word.
+    uint32_t early;
+    uint32_t out_rows;       // rows out_lp / out_tok hold (0: not checked)
 };
 
 // Row tuple of one vocab shard (lp_ragged_shard_partials), u32 words:
@@ -820,13 +826,86 @@ __device__ __forceinline__ void stage_batch_arrays(const RowsParams& p, uint32_t
     echo = s_e;
 }
 
-// Dynamic shared memory: the warps' rings, then the staged offsets.
+// The same arrays staged from the inputs alone, with the output rows derived in place: an
+// exclusive scan of (echo ? positions : 1) per batch and the plan's checks (a batch
+// range that is empty, decreasing or past T makes the offsets bad), so that nothing
+// written by lp_ragged_plan is read. Every thread of the CTA must call it; R is the
+// row count (the plan's), bad whether the plan rejects the offsets.
+template <bool EXT>
+__device__ __forceinline__ void stage_and_scan(const RowsParams& p, uint32_t* s_dyn, int tid, int nthreads,
+                                               const uint32_t*& off, const uint32_t*& loff, const uint32_t*& out_off,
+                                               const uint8_t*& echo, uint32_t& R, bool& bad) {
+    __shared__ __align__(128) uint32_t s_aux[64];  // per-warp sums, then [32]: bad flag (128-byte multiple)
+    const uint32_t B = p.B;
+    const bool var = EXT && p.loff != p.off;
+    uint32_t* s_off = s_dyn;
+    uint32_t* s_out = s_dyn + B + 1;
+    uint32_t* s_l = var ? s_dyn + 2 * (B + 1) : s_dyn;
+    uint8_t* s_e = reinterpret_cast<uint8_t*>(s_dyn + (var ? 3u : 2u) * (B + 1));
+    if (tid == 0) s_aux[32] = 0u;
+    for (uint32_t i = (uint32_t)tid; i <= B; i += (uint32_t)nthreads) {
+        s_off[i] = p.off[i];
+        if (var) s_l[i] = p.loff[i];
+        if (i < B) s_e[i] = p.echo[i];
+    }
+    __syncthreads();
+    // each thread scans a contiguous chunk of batches
+    const uint32_t per = (B + (uint32_t)nthreads - 1u) / (uint32_t)nthreads;
+    const uint32_t b0 = min((uint32_t)tid * per, B), b1 = min(b0 + per, B);
+    uint32_t sum = 0;
+    bool bd = false;
+    for (uint32_t b = b0; b < b1; ++b) {
+        const uint32_t sb = s_off[b], eb = s_off[b + 1];
+        if (eb <= sb || eb > p.T) bd = true;
+        else sum += s_e[b] ? eb - sb : 1u;
+    }
+    const int lane = tid & 31, w = tid >> 5, nw = nthreads >> 5;
+    uint32_t x = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) s_aux[w] = x;
+    if (bd) atomicOr(&s_aux[32], 1u);
+    __syncthreads();
+    if (w == 0) {
+        uint32_t v = lane < nw ? s_aux[lane] : 0u;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, v, d);
+            if (lane >= d) v += y;
+        }
+        s_aux[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    uint32_t run = x - sum + (w ? s_aux[w - 1] : 0u);
+    for (uint32_t b = b0; b < b1; ++b) {
+        s_out[b] = run;
+        const uint32_t sb = s_off[b], eb = s_off[b + 1];
+        if (!(eb <= sb || eb > p.T)) run += s_e[b] ? eb - sb : 1u;
+    }
+    if (b1 == B && b0 < b1) s_out[B] = run;
+    R = s_aux[nw - 1];
+    bad = s_aux[32] != 0u;
+    __syncthreads();
+    off = s_off;
+    out_off = s_out;
+    loff = s_l;
+    echo = s_e;
+}
+
+// Dynamic shared memory: the warps' rings, then the staged offsets. It starts where the
+// static shared memory ends, so every static shared array of the row kernels is a
+// multiple of 128 bytes: the rings then start on a 128-byte boundary and a warp's
+// 512-byte copies and 16-byte reads touch four 128-byte rows each, not five (a test
+// checks the kernels' static sizes).
 template <int U, int STAGES>
 __host__ __device__ constexpr uint32_t ring_bytes() { return (uint32_t)kWarps * STAGES * U * 512u; }
 
 template <int SLOTS, bool TOPK, int U, int STAGES, bool EXT>
 __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) {
-    extern __shared__ __align__(16) unsigned char s_raw[];
+    extern __shared__ __align__(128) unsigned char s_raw[];
     float4* rings = reinterpret_cast<float4*>(s_raw);
     uint32_t* s_dyn = reinterpret_cast<uint32_t*>(s_raw + ring_bytes<U, STAGES>());
     __shared__ float s_cx[kWarps][64];
@@ -834,22 +913,34 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t B = p.B, V = p.V, K = p.K;
 
-    pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
-    // Status, row count and the offsets are fetched in one round trip.
-    const uint32_t status = __ldcg(p.status);
-    const uint32_t R = __ldcg(p.out_off + B);
     const uint32_t* off = p.off;
     const uint32_t* loff = p.loff;
     const uint32_t* out_off = p.out_off;
     const uint8_t* echo = p.echo;
-    if (p.stage_offsets) {
-        stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kThreads, off, loff, out_off, echo);
-        __syncthreads();
+    uint32_t status, R;
+    const bool early = p.early && p.stage_offsets;
+    if (early) {
+        // rows derived here: the plan may still be running (see RowsParams::early)
+        bool bad;
+        stage_and_scan<EXT>(p, s_dyn, threadIdx.x, kThreads, off, loff, out_off, echo, R, bad);
+        status = bad ? kStatusOffsets : 0u;
+    } else {
+        pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
+        // Status, row count and the offsets are fetched in one round trip.
+        status = __ldcg(p.status);
+        R = __ldcg(p.out_off + B);
+        if (p.stage_offsets) {
+            stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kThreads, off, loff, out_off, echo);
+            __syncthreads();
+        }
     }
-    if (status & kStatusOffsets) return;  // plan rejected the offsets
+    if (status & kStatusOffsets) return;  // the plan rejects the offsets
     if (R == 0) return;
-    if (R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows)) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusOffsets);
+    if (R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows) || (p.out_rows && R > p.out_rows)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            pdl_wait();
+            atomicOr(p.status, kStatusOffsets);
+        }
         return;
     }
     const uint64_t Q = (uint64_t)R * p.nq;
@@ -883,6 +974,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
         // ---- row descriptor (identical in every lane) ---------------------------------
         const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, b, o);
         if (d.err) {
+            if (early) pdl_wait();  // before any status write
             if (q0 == 0) emit_invalid<EXT>(p, o, d.err, lane);
         } else {
             const uint32_t t = d.t;
@@ -896,6 +988,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
             sel.init(s_cx[w], s_ci[w], K);
             float xt = 0.f;
             stream_piece<SLOTS, TOPK, U, STAGES>(rowp, V, q0, q1, lane, ls, sel, t_here, t_loc, xt, ring);
+            if (early) pdl_wait();  // the plan has finished before a piece's tickets or the status are touched
 
             float C = (ls.m == neg_inf()) ? neg_inf() : ls.ref(), S = ls.sum();
             warp_lse2_reduce(C, S);
@@ -967,7 +1060,7 @@ constexpr int kQueueUnroll = LP_QUEUE_UNROLL;
 
 template <int SLOTS, bool TOPK, int U, int STAGES, int NW, bool EXT>
 __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
-    extern __shared__ __align__(16) unsigned char s_raw[];
+    extern __shared__ __align__(128) unsigned char s_raw[];
     float4* rings = reinterpret_cast<float4*>(s_raw);
     uint32_t* s_dyn = reinterpret_cast<uint32_t*>(s_raw + (size_t)NW * STAGES * U * 512u);
     __shared__ float s_cx[NW][64];
@@ -977,14 +1070,23 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t B = p.B, V = p.V, K = p.K;
 
-    pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
-    const uint32_t status = __ldcg(p.status);
-    const uint32_t R = __ldcg(p.out_off + B);
     const uint32_t* off = p.off;
     const uint32_t* loff = p.loff;
     const uint32_t* out_off = p.out_off;
     const uint8_t* echo = p.echo;
-    if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo);
+    const bool early = p.early && p.stage_offsets;
+    uint32_t status, R;
+    if (early) {
+        // rows derived here: the plan may still be running (see RowsParams::early)
+        bool bad;
+        stage_and_scan<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo, R, bad);
+        status = bad ? kStatusOffsets : 0u;
+    } else {
+        pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
+        status = __ldcg(p.status);
+        R = __ldcg(p.out_off + B);
+        if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo);
+    }
     cm.lane_max[w][lane] = neg_inf();
     // Tasks: piece `task % S` of row `task / S` (S = p.split pieces per row). The launch
     // holds two CTAs per SM and the first min(tasks, SMs) CTAs (one per SM in the
@@ -996,10 +1098,12 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     uint32_t* queue = p.counters;
     uint32_t* tickets = queue + 2;
     const bool too_many = R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows) ||
-                          (S > 1 && R > p.split_rows);
+                          (S > 1 && R > p.split_rows) || (p.out_rows && R > p.out_rows);
     const bool bad = (status & kStatusOffsets) || too_many;
     const uint32_t ntask = bad ? 0u : R * S;
     const uint32_t nA = ntask < p.num_sms ? ntask : p.num_sms;
+    // A CTA without a task of its own goes to the queue (counters): after the plan.
+    if (early && blockIdx.x >= nA) pdl_wait();
     auto next_task = [&]() -> uint32_t {  // thread 0 only
         const uint32_t rb = nA + atomicAdd(queue, 1u);
         return rb < ntask ? rb : ntask;
@@ -1060,6 +1164,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         }
         const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, lo, o);
         if (d.err) {
+            if (early) pdl_wait();  // before any status write or queue access
             if (w == 0 && piece == 0) emit_invalid<EXT>(p, o, d.err, lane);
             __syncthreads();  // every thread has read cm.row
             if (threadIdx.x == 0) cm.row = next_task();
@@ -1082,6 +1187,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         float xt = 0.f;
         stream_piece<SLOTS, TOPK, U, STAGES, NW>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr,
                                                  &cm.lane_max[0][0], w);
+        if (early) pdl_wait();  // the plan has finished before the queue, tickets or status are touched
         // The CTA's next task is asked for now, so the round trip overlaps the merges.
         uint32_t next = 0;
         if (threadIdx.x == 0) next = next_task();
@@ -1170,6 +1276,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             __syncthreads();
         }
     }
+    if (early) pdl_wait();
     if (threadIdx.x == 0) {
         __threadfence();
         if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {  // last CTA out: ready for the next call

@@ -138,9 +138,12 @@ size_t lp_ragged_workspace_size(uint32_t B, uint32_t T, uint32_t V, uint32_t lev
     return workspace_bytes_for(d->sms, levels);
 }
 
-lp_status lp_ragged_plan(const uint32_t* logit_row_offsets, const uint8_t* echo, uint32_t B, uint32_t T,
-                         uint32_t* output_row_offsets, uint32_t* host_rows_and_status, void* workspace,
-                         size_t workspace_bytes, lp_stream_t stream) {
+}  // extern "C"
+
+// The plan kernel's launch (lp_ragged_plan without the host copy).
+static lp_status plan_launch(const uint32_t* logit_row_offsets, const uint8_t* echo, uint32_t B, uint32_t T,
+                             uint32_t* output_row_offsets, void* workspace, size_t workspace_bytes,
+                             cudaStream_t s) {
     if (!logit_row_offsets || !echo || !output_row_offsets) return LP_ERR_NULL;
     if (!workspace) return LP_ERR_WORKSPACE;
     if (B == 0 || T == 0) return LP_ERR_SHAPE;
@@ -152,27 +155,41 @@ lp_status lp_ragged_plan(const uint32_t* logit_row_offsets, const uint8_t* echo,
     if (workspace_bytes < sizeof(lpk::WsHeader) + counters_bytes(g_max)) return LP_ERR_WORKSPACE;
     auto* hdr = static_cast<lpk::WsHeader*>(workspace);
     auto* counters = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) + sizeof(lpk::WsHeader));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     lpk::k_plan<<<1, lpk::kPlanThreads, 0, s>>>(logit_row_offsets, echo, B, T, output_row_offsets, hdr, counters,
                                                g_max);
     if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
-    if (host_rows_and_status) {
-        // header words {status, rows} -> host {rows, status}
-        if (cudaMemcpyAsync(host_rows_and_status, &hdr->rows, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-            cudaMemcpyAsync(host_rows_and_status + 1, &hdr->status, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-            return LP_ERR_CUDA;
-    }
     return LP_OK;
+}
+
+// Header words {status, rows} -> host {rows, status}.
+static lp_status copy_rows_and_status(uint32_t* host_rows_and_status, void* workspace, cudaStream_t s) {
+    auto* hdr = static_cast<lpk::WsHeader*>(workspace);
+    if (cudaMemcpyAsync(host_rows_and_status, &hdr->rows, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(host_rows_and_status + 1, &hdr->status, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return LP_ERR_CUDA;
+    return LP_OK;
+}
+
+extern "C" {
+
+lp_status lp_ragged_plan(const uint32_t* logit_row_offsets, const uint8_t* echo, uint32_t B, uint32_t T,
+                         uint32_t* output_row_offsets, uint32_t* host_rows_and_status, void* workspace,
+                         size_t workspace_bytes, lp_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const lp_status st = plan_launch(logit_row_offsets, echo, B, T, output_row_offsets, workspace, workspace_bytes, s);
+    if (st != LP_OK || !host_rows_and_status) return st;
+    return copy_rows_and_status(host_rows_and_status, workspace, s);
 }
 
 // The row kernels' launch: writes rows (tuples == nullptr) or, for a vocab shard,
 // one row tuple per output row with ids offset by vocab_base.
-static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V, const uint32_t* logit_row_offsets,
-                              const uint32_t* input_row_offsets, uint32_t T, uint32_t B, const uint32_t* tokens,
-                              const uint32_t* sampled_tokens, const uint32_t* output_row_offsets, const uint8_t* echo,
-                              const float* temperatures, uint32_t levels, float* out_logprobs, uint32_t* out_tokens,
-                              void* tuples, uint32_t vocab_base, uint32_t tuple_rows, void* workspace,
-                              size_t workspace_bytes, lp_stream_t stream) {
+// The row kernels' host checks (every one that can fail before a launch).
+static lp_status compute_checks(const float* logits, uint32_t T_logits, uint32_t V, const uint32_t* logit_row_offsets,
+                                const uint32_t* input_row_offsets, uint32_t T, uint32_t B, const uint32_t* tokens,
+                                const uint32_t* sampled_tokens, const uint32_t* output_row_offsets,
+                                const uint8_t* echo, uint32_t levels, const float* out_logprobs,
+                                const uint32_t* out_tokens, const void* tuples, const void* workspace,
+                                size_t workspace_bytes, DeviceInfo** dev_info) {
     if (!logits || !logit_row_offsets || !tokens || !sampled_tokens || !output_row_offsets || !echo ||
         (!tuples && (!out_logprobs || !out_tokens)))
         return LP_ERR_NULL;
@@ -183,9 +200,22 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     if (((uintptr_t)logits & 3u) != 0) return LP_ERR_SHAPE;
     if (((uintptr_t)workspace & 255u) != 0) return LP_ERR_WORKSPACE;
     int dev;
+    if (!device_info(&dev, dev_info)) return LP_ERR_CUDA;
+    if (workspace_bytes < workspace_bytes_for((*dev_info)->sms, levels)) return LP_ERR_WORKSPACE;
+    return LP_OK;
+}
+
+static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V, const uint32_t* logit_row_offsets,
+                              const uint32_t* input_row_offsets, uint32_t T, uint32_t B, const uint32_t* tokens,
+                              const uint32_t* sampled_tokens, const uint32_t* output_row_offsets, const uint8_t* echo,
+                              const float* temperatures, uint32_t levels, float* out_logprobs, uint32_t* out_tokens,
+                              void* tuples, uint32_t vocab_base, uint32_t tuple_rows, uint32_t out_rows, bool early,
+                              void* workspace, size_t workspace_bytes, lp_stream_t stream) {
     DeviceInfo* d;
-    if (!device_info(&dev, &d)) return LP_ERR_CUDA;
-    if (workspace_bytes < workspace_bytes_for(d->sms, levels)) return LP_ERR_WORKSPACE;
+    const lp_status chk = compute_checks(logits, T_logits, V, logit_row_offsets, input_row_offsets, T, B, tokens,
+                                         sampled_tokens, output_row_offsets, echo, levels, out_logprobs, out_tokens,
+                                         tuples, workspace, workspace_bytes, &d);
+    if (chk != LP_OK) return chk;
 
     const uint32_t K = (1u << levels) - 1u;
     const uint32_t W = levels ? (1u << levels) : 1u;
@@ -223,6 +253,8 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     p.num_sms = (uint32_t)d->sms;
     p.split = 1;
     p.split_rows = 0;
+    p.early = early ? 1u : 0u;
+    p.out_rows = out_rows;
 
     const uint32_t staged_arrays = (p.loff != p.off) ? 3u : 2u;
     const size_t smem =
@@ -294,8 +326,8 @@ lp_status lp_ragged_compute_ex(const float* logits, uint32_t T_logits, uint32_t 
                                uint32_t levels, float* out_logprobs, uint32_t* out_tokens, void* workspace,
                                size_t workspace_bytes, lp_stream_t stream) {
     return compute_impl(logits, T_logits, V, logit_row_offsets, input_row_offsets, T, B, tokens, sampled_tokens,
-                        output_row_offsets, echo, temperatures, levels, out_logprobs, out_tokens, nullptr, 0u, 0u,
-                        workspace, workspace_bytes, stream);
+                        output_row_offsets, echo, temperatures, levels, out_logprobs, out_tokens, nullptr, 0u, 0u, 0u,
+                        false, workspace, workspace_bytes, stream);
 }
 
 lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const uint32_t* logit_row_offsets,
@@ -304,8 +336,34 @@ lp_status lp_ragged_compute(const float* logits, uint32_t T, uint32_t V, const u
                             float* out_logprobs, uint32_t* out_tokens, void* workspace, size_t workspace_bytes,
                             lp_stream_t stream) {
     return compute_impl(logits, T, V, logit_row_offsets, nullptr, T, B, tokens, sampled_tokens, output_row_offsets,
-                        echo, nullptr, levels, out_logprobs, out_tokens, nullptr, 0u, 0u, workspace,
+                        echo, nullptr, levels, out_logprobs, out_tokens, nullptr, 0u, 0u, 0u, false, workspace,
                         workspace_bytes, stream);
+}
+
+lp_status lp_ragged_step(const float* logits, uint32_t T_logits, uint32_t V, const uint32_t* logit_row_offsets,
+                         const uint32_t* input_row_offsets, uint32_t T, uint32_t B, const uint32_t* tokens,
+                         const uint32_t* sampled_tokens, const uint8_t* echo, const float* temperatures,
+                         uint32_t levels, uint32_t* output_row_offsets, uint32_t* host_rows_and_status,
+                         float* out_logprobs, uint32_t* out_tokens, uint32_t out_rows, void* workspace,
+                         size_t workspace_bytes, lp_stream_t stream) {
+    // every check of both launches first, so that an error leaves nothing enqueued
+    if (out_rows == 0) return LP_ERR_SHAPE;
+    DeviceInfo* d;
+    const lp_status chk = compute_checks(logits, T_logits, V, logit_row_offsets, input_row_offsets, T, B, tokens,
+                                         sampled_tokens, output_row_offsets, echo, levels, out_logprobs, out_tokens,
+                                         nullptr, workspace, workspace_bytes, &d);
+    if (chk != LP_OK) return chk;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The plan is an ordinary launch (after everything before it on the stream); the row
+    // kernel follows it directly, so it may read its inputs before the plan has finished.
+    lp_status st = plan_launch(input_row_offsets ? input_row_offsets : logit_row_offsets, echo, B, T,
+                               output_row_offsets, workspace, workspace_bytes, s);
+    if (st != LP_OK) return st;
+    st = compute_impl(logits, T_logits, V, logit_row_offsets, input_row_offsets, T, B, tokens, sampled_tokens,
+                      output_row_offsets, echo, temperatures, levels, out_logprobs, out_tokens, nullptr, 0u, 0u,
+                      out_rows, true, workspace, workspace_bytes, stream);
+    if (st != LP_OK || !host_rows_and_status) return st;
+    return copy_rows_and_status(host_rows_and_status, workspace, s);  // rows, and the step's status
 }
 
 uint32_t lp_ragged_tuple_bytes(uint32_t levels) {
@@ -325,7 +383,7 @@ lp_status lp_ragged_shard_partials(const float* logits, uint32_t T_logits, uint3
     if ((uint64_t)vocab_base + V_shard >= 0x7FFFFFFFull) return LP_ERR_SHAPE;
     return compute_impl(logits, T_logits, V_shard, logit_row_offsets, input_row_offsets, T, B, tokens,
                         sampled_tokens, output_row_offsets, echo, temperatures, levels, nullptr, nullptr, tuples,
-                        vocab_base, rows_capacity, workspace, workspace_bytes, stream);
+                        vocab_base, rows_capacity, 0u, false, workspace, workspace_bytes, stream);
 }
 
 lp_status lp_ragged_shard_merge(const void* tuples, uint32_t P, uint32_t rows_capacity, uint32_t V,

@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert set(declared_functions()) >= {"lp_ragged_workspace_size", "lp_ragged_plan", "lp_ragged_compute",
-                                         "lp_ragged_compute_ex", "lp_ragged_read_status", "lp_ragged_strerror"}
+                                         "lp_ragged_compute_ex", "lp_ragged_step", "lp_ragged_read_status",
+                                         "lp_ragged_strerror"}
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -89,6 +90,29 @@ def test_compute_ex_host_checks(lib):
     assert _compute_ex(lib, ws=FAKE + 64) == LP_ERR_WORKSPACE
 
 
+def _step(lib, logits=FAKE, T_logits=4, V=100, loff=FAKE, ioff=None, T=4, B=2, tokens=FAKE, sampled=FAKE, echo=FAKE,
+          tau=None, levels=3, out_off=FAKE, host=None, out_lp=FAKE, out_tok=FAKE, rows=4, ws=FAKE, ws_bytes=1 << 20):
+    return lib.lp_ragged_step(logits, T_logits, V, loff, ioff, T, B, tokens, sampled, echo, tau, levels, out_off,
+                              host, out_lp, out_tok, rows, ws, ws_bytes, None)
+
+
+def test_step_host_checks(lib):
+    # every check of the plan and the reduction comes before either launch
+    assert _step(lib, rows=0) == LP_ERR_SHAPE
+    assert _step(lib, logits=None) == LP_ERR_NULL
+    assert _step(lib, loff=None) == LP_ERR_NULL
+    assert _step(lib, out_off=None) == LP_ERR_NULL
+    assert _step(lib, echo=None) == LP_ERR_NULL
+    assert _step(lib, out_tok=None) == LP_ERR_NULL
+    assert _step(lib, ws=None) == LP_ERR_WORKSPACE
+    assert _step(lib, levels=7) == LP_ERR_LEVELS
+    assert _step(lib, T=6) == LP_ERR_SHAPE                    # no input offsets: T must equal T_logits
+    assert _step(lib, B=0) == LP_ERR_SHAPE
+    assert _step(lib, V=0) == LP_ERR_SHAPE
+    assert _step(lib, logits=FAKE + 1) == LP_ERR_SHAPE
+    assert _step(lib, ws=FAKE + 64) == LP_ERR_WORKSPACE
+
+
 def test_shard_entry_points_host_checks(lib):
     assert lib.lp_ragged_tuple_bytes(3) == 80 and lib.lp_ragged_tuple_bytes(6) == 528
     assert lib.lp_ragged_tuple_bytes(0) == 16 and lib.lp_ragged_tuple_bytes(7) == 0
@@ -135,3 +159,23 @@ def test_package_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(lp._build, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         lp.load()
+
+
+def test_row_kernels_static_shared_memory_keeps_rings_aligned(tmp_path, capfd):
+    # The rings live in dynamic shared memory, which starts where a kernel's static shared
+    # memory ends: a static size off a multiple of 128 bytes would make every warp's
+    # 512-byte copies and 16-byte reads touch five 128-byte rows instead of four.
+    from ragged_log_probs_gb300 import _build
+    _build.build(force=True, ptxas_verbose=True, out=str(tmp_path / "liblp_check.so"))
+    report = capfd.readouterr().err
+    sizes, kernel = {}, None
+    for line in report.splitlines():
+        m = re.search(r"Compiling entry function '(\S+)'", line)
+        if m:
+            kernel = m.group(1)
+            continue
+        m = re.search(r"Used \d+ registers.*?(\d+) bytes smem", line)
+        if m and kernel and "k_rows" in kernel:
+            sizes[kernel] = int(m.group(1))
+    assert len(sizes) >= 12, report[-2000:]
+    assert all(v % 128 == 0 for v in sizes.values()), sizes
