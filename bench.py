@@ -66,9 +66,9 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 134999040, "source_hash": "cb768fcaba10c317",
+    "decode": {"bytes_per_launch": 135005184, "source_hash": "e47ffcdc2f318c1d",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 903291136, "source_hash": "cb768fcaba10c317",
+    "prefill": {"bytes_per_launch": 903563776, "source_hash": "e47ffcdc2f318c1d",
                 "capture": "profiles/k_rows_prefill.md"},
 }
 
@@ -99,8 +99,10 @@ def _code_only(text: str) -> str:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernels' device code (the .cuh sources, comments stripped): the host
+    file picks kernels and shapes, the device code decides what one launch moves."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "ragged_log_probs_gb300", "csrc", "*"))):
+    for f in sorted(glob.glob(os.path.join(ROOT, "ragged_log_probs_gb300", "csrc", "*.cuh"))):
         with open(f, encoding="utf-8") as fh:
             h.update(os.path.basename(f).encode())
             h.update(_code_only(fh.read()).encode())
@@ -109,10 +111,10 @@ def kernel_source_hash() -> str:
 
 def uses_row_queue(rows_bound: int, V: int) -> bool:
     """The library's kernel choice: the row-queue kernel when at most three rows per SM
-    can come out, or at most five of at most 40K logits; else the warp-range kernel."""
+    can come out; else the warp-range kernel."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return rows_bound <= 3 * sms or (rows_bound <= 5 * sms and V <= 40960)
+    return rows_bound <= 3 * sms
 
 
 def algorithmic_bytes(R: int, V: int, W: int, B: int) -> int:
@@ -512,7 +514,7 @@ def run_ours(args, rank: int, world: int, dist):
                    "levels": levels, "rows_per_gpu": R, "parallelism": f"replicas x{world} (independent batches)",
                    "l2": f"inputs larger than L2: {n_copies} rotating logits copies of {lbytes / 1e6:.0f} MB "
                          f"(L2 {l2 / 1e6:.0f} MB)",
-                   "launch": "the K timed steps (plan + compute each) replayed from one CUDA graph"},
+                   "launch": "the K timed steps (lp_ragged_step: plan + row kernel; vocab8: plan, partials, merge) replayed from one CUDA graph"},
         "hbm_gbs_step": round(alg * world / (ms_step / 1e3) / 1e9, 1),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (3 if sharded else 2) * args.steps, "clocks": clocks,

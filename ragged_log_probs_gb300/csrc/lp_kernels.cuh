@@ -1028,8 +1028,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
 }
 
 // ---------------------------------------------------------------------------------
-// Few rows (up to three per SM, or five when rows are at most 40K logits; e.g. next-token
-// logits for a decode batch): CTAs of NW warps take tasks; a task is a whole row, or, when
+// Few rows (up to three per SM; e.g. next-token logits for a decode batch): CTAs of NW warps take tasks; a task is a whole row, or, when
 // there are fewer rows than twice the SMs, one of S contiguous pieces of a row
 // (split-vocab: S = min(2*SMs / rows, row length / 16 KB, 64), chosen on the host). The
 // CTA's warps split the task into NW contiguous parts and merge their results in shared

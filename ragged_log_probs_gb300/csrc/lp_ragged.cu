@@ -261,9 +261,8 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
         kRingBytes + (p.stage_offsets ? (size_t)staged_arrays * (B + 1u) * sizeof(uint32_t) + ((B + 3u) & ~3u) : 0);
 
     // Row queue when even all-echo input (R <= T, and R <= T_logits) gives at most three
-    // rows per SM, or at most five of at most 40K logits; otherwise warp-owned ranges of
-    // the row space (the two kernels give the same result; the switch points come from
-    // timing both on next-token shapes).
+    // rows per SM; otherwise warp-owned ranges of the row space (the two kernels give the
+    // same result; the switch point comes from timing both on next-token shapes).
     // Plain instantiation unless an extended input is given (it compiles without them).
     const bool ext = input_row_offsets != nullptr || temperatures != nullptr || tuples != nullptr;
     int v = variant_of(levels) + (ext ? 6 : 0);
@@ -272,7 +271,7 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;  // occ <= kMaxCtasPerSm
     const char* force = std::getenv("LP_RAGGED_KERNEL");  // test hook: "warp" or "queue"
     const uint32_t r_max = T < T_logits ? T : T_logits;
-    bool queue = r_max <= 3u * (uint32_t)d->sms || (r_max <= 5u * (uint32_t)d->sms && V <= 40960u);
+    bool queue = r_max <= 3u * (uint32_t)d->sms;
     if (force && std::strcmp(force, "warp") == 0) queue = false;
     if (force && std::strcmp(force, "queue") == 0) queue = true;
     size_t launch_smem = smem;
