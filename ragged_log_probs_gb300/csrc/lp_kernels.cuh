@@ -54,7 +54,10 @@ namespace lpk {
 #endif
 
 
-constexpr int kWarps = 8;
+#ifndef LP_WARPS
+#define LP_WARPS 8  // warps per CTA of the warp-range kernel
+#endif
+constexpr int kWarps = LP_WARPS;
 constexpr int kThreads = kWarps * 32;
 #ifndef LP_THR_EVERY
 #define LP_THR_EVERY 8
