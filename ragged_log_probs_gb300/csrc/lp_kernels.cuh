@@ -54,10 +54,7 @@ namespace lpk {
 #endif
 
 
-#ifndef LP_WARPS
-#define LP_WARPS 8  // warps per CTA of the warp-range kernel
-#endif
-constexpr int kWarps = LP_WARPS;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 #ifndef LP_THR_EVERY
 #define LP_THR_EVERY 8
