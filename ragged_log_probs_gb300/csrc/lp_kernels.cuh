@@ -475,13 +475,32 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
             // every kThrEvery blocks.
             if (refresh_due(blk)) {
                 float lm = ls.m;
+                uint32_t kk = sel.K;
                 if constexpr (TABW > 0) {
                     volatile float* tab = lane_tab;
                     tab[w * 32 + lane] = lm;
+                    if (kk <= 15u || blk < kThrEvery) {
 #pragma unroll
-                    for (int j = 0; j < TABW; ++j) lm = fmaxf(lm, tab[j * 32 + lane]);
+                        for (int j = 0; j < TABW; ++j) lm = fmaxf(lm, tab[j * 32 + lane]);
+                    } else {
+                        // K = 16..31: the K-th of 32 column maxima is nearly their minimum.
+                        // Each lane position's second best across the warps instead: the
+                        // k-th largest of those stands above 2k distinct elements (the k
+                        // second bests and the k bests above them), so k = ceil(K/2). Not on
+                        // the first blocks, while few warps have published their maxima
+                        // (the second bests are then mostly -inf).
+                        float hi = neg_inf(), lo = neg_inf();
+#pragma unroll
+                        for (int j = 0; j < TABW; ++j) {
+                            const float v2 = tab[j * 32 + lane];
+                            lo = fmaxf(lo, fminf(hi, v2));
+                            hi = fmaxf(hi, v2);
+                        }
+                        lm = lo;
+                        kk = (kk + 1u) >> 1;
+                    }
                 }
-                sel.thr = fmaxf(sel.thr, kth_largest32(lm, sel.K, lane));
+                sel.thr = fmaxf(sel.thr, kth_largest32(lm, kk, lane));
                 if (shared_thr != nullptr) {  // warps on the same row share their thresholds
                     if (lane == 0 && sel.thr != neg_inf()) atomicMax(shared_thr, f2ord(sel.thr));
                     sel.thr = fmaxf(sel.thr, ord2f(*(volatile uint32_t*)shared_thr));

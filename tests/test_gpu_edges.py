@@ -264,6 +264,21 @@ def test_kernel_choice_boundary(B, V):
     parity.check_batch(b, rows=parity.sample_rows(B, 40, seed=B), what=f"B={B} V={V}")
 
 
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
+@pytest.mark.parametrize("quantised", [False, True])
+def test_levels5_long_rows(kernel, quantised, monkeypatch):
+    # top-31 over long rows: the row queue bounds it by the 16th largest of each lane
+    # position's second-best lane maximum across its warps; quantised logits put many
+    # elements exactly on that bound.
+    monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
+    g = torch.Generator().manual_seed(55)
+    x = torch.randn(24, 128256, generator=g) * 3
+    if quantised:
+        x = torch.round(x * 2) / 2
+    b = workloads.make_custom_batch(x.cuda(), [1] * 24, [0] * 24, 5, seed=55)
+    parity.check_batch(b, what=f"levels 5/{kernel}/{'quantised' if quantised else 'normal'}")
+
+
 def test_decode_full_size_levels6_sampled():
     b = workloads.make_batch("decode", "cuda", levels=6)
     parity.check_batch(b, rows=parity.sample_rows(b.B, 16, seed=6), what="decode levels 6")
