@@ -226,6 +226,33 @@ struct LaneSum {
         }
         nc = -c_new;
     }
+    // The terms of one ring block under the current reference, summed in pairs (packed).
+    template <int U>
+    __device__ __forceinline__ float2 block_terms(const float4 (&v)[U]) const {
+        const float2 l2e = make_float2(k, k), mc = make_float2(nc, nc);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float2 y0 = ffma2(make_float2(v[u].x, v[u].y), l2e, mc);
+            const float2 y1 = ffma2(make_float2(v[u].z, v[u].w), l2e, mc);
+            acc = fadd2(acc, fadd2(make_float2(ex2(y0.x), ex2(y0.y)), make_float2(ex2(y1.x), ex2(y1.y))));
+        }
+        return acc;
+    }
+    // Account for a block whose largest logit is bm and add its terms. They are computed
+    // under the current reference without waiting for bm, and only in the rare case that
+    // the reference moves up (the first finite block, or a maximum beyond the headroom)
+    // computed again after the rebase.
+    template <int U>
+    __device__ __forceinline__ void add_block(const float4 (&v)[U], float bm) {
+        m = fmaxf(m, bm);
+        float2 acc = block_terms<U>(v);
+        if (fmaf(bm, k, nc) > kHeadroom) {
+            rebase(bm);
+            acc = block_terms<U>(v);
+        }
+        s = fadd2(s, acc);
+    }
     // Add the terms of four logits: two packed FMAs, four EX2, two packed adds.
     __device__ __forceinline__ void add4(const float4& v) {
         const float2 l2e = make_float2(k, k), mc = make_float2(nc, nc);
@@ -463,9 +490,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
 #pragma unroll
         for (int u = 1; u + 1 < U; u += 2) bm = max3(bm, mu[u], mu[u + 1]);
         if ((U & 1) == 0) bm = fmaxf(bm, mu[U - 1]);
-        ls.note(bm);
-#pragma unroll
-        for (int u = 0; u < U; ++u) ls.add4(v[u]);
+        ls.add_block<U>(v, bm);
 
         if constexpr (TOPK && SLOTS == 1) {
             // The K-th largest of the 32 lanes' running maxima is the value of K distinct
