@@ -1074,7 +1074,8 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
 // ---------------------------------------------------------------------------------
 // Few rows (up to three per SM; e.g. next-token logits for a decode batch): CTAs of NW warps take tasks; a task is a whole row, or, when
 // there are fewer rows than twice the SMs, one of S contiguous pieces of a row
-// (split-vocab: S = min(2*SMs / rows, row length / 16 KB, 64), chosen on the host). The
+// (split-vocab, chosen on the host: S = min(2*SMs / rows, row length / 42 KB, 64) for rows
+// of 192 KB or more). The
 // CTA's warps split the task into NW contiguous parts and merge their results in shared
 // memory; a whole row is written at once, a piece is published to the workspace and the
 // CTA that takes the row's last ticket merges the S pieces with all its warps (each warp

@@ -18,7 +18,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kMaxCtasPerSm = 4;           // launch cap; sizes the workspace
 constexpr uint32_t kMinPieceVec = 1024;         // 16 KB of logits per warp at least
-constexpr uint32_t kMinSplitVec = 1024;         // 16 KB of logits per row-queue piece at least
+constexpr uint32_t kMinSplitVec = 2688;         // 42 KB of logits per row-queue piece at least
+constexpr uint32_t kSplitRowVec = 12288;        // rows shorter than 192 KB are not split
 constexpr uint32_t kMaxSplit = 64;              // pieces per row in the row-queue kernel
 constexpr uint32_t kStageOffsetsMax = 2048;     // stage off/out_off in smem when B+1 <= this
 constexpr uint32_t kUnroll = LP_UNROLL;
@@ -285,9 +286,12 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
         occ = occupancy(d, v, launch_smem);
         if (occ == 0) return LP_ERR_CUDA;
         grid = (uint32_t)d->sms * (uint32_t)occ;
-        // split-vocab for small batches: pieces per row so that the tasks number about two per SM
+        // split-vocab for small batches: pieces per row so that the tasks number about two per
+        // SM, of at least 42 KB each, and only for rows of 192 KB or more (a piece costs a
+        // publish, a ticket and a merge, ~5 us, which pays only where one CTA would otherwise
+        // stream a long row)
         uint32_t S = (2u * (uint32_t)d->sms) / (r_max ? r_max : 1u);
-        const uint32_t by_len = p.nq / kMinSplitVec;
+        const uint32_t by_len = p.nq >= kSplitRowVec ? p.nq / kMinSplitVec : 1u;
         if (S > by_len) S = by_len;
         if (S > kMaxSplit) S = kMaxSplit;
         const char* fs = std::getenv("LP_RAGGED_SPLIT");  // test hook: pieces per row
