@@ -22,7 +22,7 @@ What it computes (the plain definition, written out, slow on purpose):
   logprob 来自哪里": a prompt position scores the next prompt token; the decode
   step scores the sampled token.
 
-Readings taken where the pages are silent (each is also listed in the design doc):
+Readings taken where the pages are silent:
 
 * Non-echo batches read the LAST logits row of their sequence (for next-token
   logits with ``off = arange(B+1)`` that row is the only one).
