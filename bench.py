@@ -66,9 +66,9 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 135005184, "source_hash": "e47ffcdc2f318c1d",
+    "decode": {"bytes_per_launch": 134720256, "source_hash": "dea5adcab13a080f",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 903563776, "source_hash": "e47ffcdc2f318c1d",
+    "prefill": {"bytes_per_launch": 903236352, "source_hash": "dea5adcab13a080f",
                 "capture": "profiles/k_rows_prefill.md"},
 }
 
