@@ -801,6 +801,34 @@ __device__ __forceinline__ bool take_ticket(uint32_t* counters, uint64_t w0, uin
     return last;
 }
 
+// Batch of output row o: the last b < B with out_off[b] <= o (out_off[0] = 0 and the
+// offsets increase: every batch has at least one output row). With the offsets in shared
+// memory the warp looks at 32 evenly spaced entries, then at the entries of the stride the
+// first round chose (at most 64 for B <= 2047): two dependent loads, against ~log2(B) for a
+// binary search. Warp-uniform: every lane calls it with the same o.
+__device__ __forceinline__ uint32_t batch_of_row(const uint32_t* out_off, uint32_t B, uint32_t o, bool staged,
+                                                 int lane) {
+    if (!staged) {
+        uint32_t lo = 0, hi = B;
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (out_off[mid] <= o) lo = mid; else hi = mid;
+        }
+        return lo;
+    }
+    const uint32_t step = (B + 31u) >> 5;
+    const uint32_t i = (uint32_t)lane * step;
+    const unsigned first = __ballot_sync(kFull, i < B && out_off[i] <= o);  // lanes 0.. (lane 0 always)
+    const uint32_t base = (31u - (uint32_t)__clz(first | 1u)) * step;
+    uint32_t best = base;
+    for (uint32_t j0 = 0; j0 < step; j0 += 32u) {
+        const uint32_t j = base + j0 + (uint32_t)lane;
+        const unsigned hit = __ballot_sync(kFull, j0 + (uint32_t)lane < step && j < B && out_off[j] <= o);
+        if (hit) best = base + j0 + (31u - (uint32_t)__clz(hit));
+    }
+    return best;
+}
+
 // Where one output row reads and what it scores. Output row o of batch b is the
 // (o - out_off[b])-th of the batch's last cnt positions; position r scores token r+1
 // of the same sequence, the last position the batch's sampled token. Its logits row
@@ -1003,12 +1031,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
     uint32_t o = (uint32_t)(g0 / p.nq);
     const uint32_t o_first = o;
     uint32_t q0 = (uint32_t)(g0 - (uint64_t)o * p.nq);
-    uint32_t lo = 0, hi = B;  // batch of row o: last b with out_off[b] <= o
-    while (hi - lo > 1) {
-        const uint32_t mid = (lo + hi) >> 1;
-        if (out_off[mid] <= o) lo = mid; else hi = mid;
-    }
-    uint32_t b = lo;
+    uint32_t b = batch_of_row(out_off, B, o, p.stage_offsets != 0u, lane);  // batch of row o
     float4* ring = rings + (size_t)w * STAGES * U * 32;
 
     for (uint64_t g = g0; g < g1;) {
@@ -1200,12 +1223,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     for (;;) {
         const uint32_t task = cm.row;
         if (task >= ntask) break;
-        const uint32_t o = task / S, piece = task - o * S;
-        uint32_t lo = 0, hi = B;  // batch of row o
-        while (hi - lo > 1) {
-            const uint32_t mid = (lo + hi) >> 1;
-            if (out_off[mid] <= o) lo = mid; else hi = mid;
-        }
+        const uint32_t o = S == 1u ? task : task / S, piece = task - o * S;
+        const uint32_t lo = batch_of_row(out_off, B, o, p.stage_offsets != 0u, lane);
         const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, lo, o);
         if (d.err) {
             if (early) pdl_wait();  // before any status write or queue access
@@ -1218,8 +1237,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         const uint32_t t = d.t;
         const uint32_t t_loc = EXT ? t - p.vocab_base : t;  // column of the target in this shard
         const float* rowp = d.rowp;
-        const uint32_t pq0 = (uint32_t)(((uint64_t)p.nq * piece) / S);
-        const uint32_t pq1 = (uint32_t)(((uint64_t)p.nq * (piece + 1)) / S);
+        const uint32_t pq0 = S == 1u ? 0u : (uint32_t)(((uint64_t)p.nq * piece) / S);
+        const uint32_t pq1 = S == 1u ? p.nq : (uint32_t)(((uint64_t)p.nq * (piece + 1)) / S);
         const uint32_t wq0 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * w) / NW);
         const uint32_t wq1 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * (w + 1)) / NW);
         bool t_here;
