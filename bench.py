@@ -66,9 +66,9 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 134720256, "source_hash": "dea5adcab13a080f",
+    "decode": {"bytes_per_launch": 134979584, "source_hash": "eeee33f93566ce8e",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 903236352, "source_hash": "dea5adcab13a080f",
+    "prefill": {"bytes_per_launch": 903159296, "source_hash": "eeee33f93566ce8e",
                 "capture": "profiles/k_rows_prefill.md"},
 }
 
