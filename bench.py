@@ -66,9 +66,9 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 134979584, "source_hash": "eeee33f93566ce8e",
+    "decode": {"bytes_per_launch": 134591488, "source_hash": "c08e5e102537df4c",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 903159296, "source_hash": "eeee33f93566ce8e",
+    "prefill": {"bytes_per_launch": 903232256, "source_hash": "c08e5e102537df4c",
                 "capture": "profiles/k_rows_prefill.md"},
 }
 

@@ -1356,6 +1356,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
 // under (logit desc, global id asc), and the target logit comes from the shard that
 // holds it.
 constexpr int kMergeWarps = 8;
+constexpr int kMergeBatch = 8;  // shard lists loaded together (the first batch before the headers)
 
 template <int SLOTS, bool TOPK>
 __global__ void __launch_bounds__(kMergeWarps * 32) k_shard_merge(RowsParams p, const unsigned char* tuples,
@@ -1370,6 +1371,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32) k_shard_merge(RowsParams p, 
     const uint32_t nw = gridDim.x * kMergeWarps;
     for (uint32_t o = blockIdx.x * kMergeWarps + (threadIdx.x >> 5); o < R; o += nw) {
         const unsigned char* row0 = tuples + (size_t)o * p.stride;
+        // The shards' sorted lists do not depend on the headers: the first batch is loaded
+        // now, so the row costs about one memory latency for up to kMergeBatch shards.
+        float bx[kMergeBatch][SLOTS];
+        uint32_t bi[kMergeBatch][SLOTS];
+        if constexpr (TOPK) {
+#pragma unroll
+            for (int q = 0; q < kMergeBatch; ++q)
+                if ((uint32_t)q < P)
+                    load_piece_list<SLOTS>(reinterpret_cast<const uint32_t*>(row0 + q * shard_bytes), p.K, lane, bx[q],
+                                           bi[q]);
+        }
         float C = neg_inf(), S = 0.f, xt = 0.f;
         bool has_xt = false, bad = false;
         uint32_t t = 0;
@@ -1394,11 +1406,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32) k_shard_merge(RowsParams p, 
         WarpList<SLOTS> L;
         L.reset();
         if constexpr (TOPK) {
-            for (uint32_t j = 0; j < P; ++j) {
-                float cx[SLOTS];
-                uint32_t ci[SLOTS];
-                load_piece_list<SLOTS>(reinterpret_cast<const uint32_t*>(row0 + j * shard_bytes), p.K, lane, cx, ci);
-                merge_lists<SLOTS>(L.x, L.id, cx, ci, lane);
+            for (uint32_t j0 = 0; j0 < P; j0 += kMergeBatch) {
+                if (j0 != 0) {
+#pragma unroll
+                    for (int q = 0; q < kMergeBatch; ++q)
+                        if (j0 + q < P)
+                            load_piece_list<SLOTS>(reinterpret_cast<const uint32_t*>(row0 + (j0 + q) * shard_bytes),
+                                                   p.K, lane, bx[q], bi[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < kMergeBatch; ++q)
+                    if (j0 + q < P) merge_lists<SLOTS>(L.x, L.id, bx[q], bi[q], lane);
             }
         }
         float kk = kLog2e;
