@@ -279,6 +279,22 @@ def test_levels5_long_rows(kernel, quantised, monkeypatch):
     parity.check_batch(b, what=f"levels 5/{kernel}/{'quantised' if quantised else 'normal'}")
 
 
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
+@pytest.mark.parametrize("B", [1025, 2047])
+def test_many_batches_staged_row_lookup(kernel, B, monkeypatch):
+    # Up to 2047 batches the offsets sit in shared memory and a row's batch is found with two
+    # ballot rounds (at B = 2047 each lane's stride is 64 entries: two rounds of 32 lanes).
+    # Uneven echo counts make the output offsets jump unevenly.
+    monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
+    rng = np.random.default_rng(B)
+    lengths = rng.integers(1, 4, size=B)
+    echo = (rng.random(B) < 0.5).astype(np.int64)
+    g = torch.Generator().manual_seed(B)
+    x = torch.randn(int(lengths.sum()), 257, generator=g).cuda()
+    b = _custom(x, lengths.tolist(), echo.tolist(), 3, seed=B)
+    parity.check_batch(b, what=f"B={B}/{kernel}")
+
+
 def test_decode_full_size_levels6_sampled():
     b = workloads.make_batch("decode", "cuda", levels=6)
     parity.check_batch(b, rows=parity.sample_rows(b.B, 16, seed=6), what="decode levels 6")
