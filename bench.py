@@ -70,6 +70,10 @@ NCU_TRAFFIC = {
                "capture": "profiles/k_rows_cta_decode.md"},
     "prefill": {"bytes_per_launch": 903232256, "source_hash": "c08e5e102537df4c",
                 "capture": "profiles/k_rows_prefill.md"},
+    "mixed": {"bytes_per_launch": 3336400128, "source_hash": "c08e5e102537df4c",
+              "capture": "profiles/k_rows_mixed_wide_dram.md"},
+    "wide": {"bytes_per_launch": 22139089152, "source_hash": "c08e5e102537df4c",
+             "capture": "profiles/k_rows_mixed_wide_dram.md"},
 }
 
 
