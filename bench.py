@@ -66,13 +66,13 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 134591488, "source_hash": "c08e5e102537df4c",
+    "decode": {"bytes_per_launch": 134618880, "source_hash": "b0e63e470d1f1323",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 903232256, "source_hash": "c08e5e102537df4c",
+    "prefill": {"bytes_per_launch": 903196416, "source_hash": "b0e63e470d1f1323",
                 "capture": "profiles/k_rows_prefill.md"},
-    "mixed": {"bytes_per_launch": 3336400128, "source_hash": "c08e5e102537df4c",
+    "mixed": {"bytes_per_launch": 3336375040, "source_hash": "b0e63e470d1f1323",
               "capture": "profiles/k_rows_mixed_wide_dram.md"},
-    "wide": {"bytes_per_launch": 22139089152, "source_hash": "c08e5e102537df4c",
+    "wide": {"bytes_per_launch": 22139949312, "source_hash": "b0e63e470d1f1323",
              "capture": "profiles/k_rows_mixed_wide_dram.md"},
 }
 

@@ -81,6 +81,12 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Bulk prefetch of the bytes [gptr, gptr + bytes) into L2, a hint with no completion to
+// wait for (gptr 16-byte aligned, bytes a multiple of 16, the range inside one allocation).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* gptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ bool better(float xa, uint32_t ia, float xb, uint32_t ib) {
     return xa > xb || (xa == xb && ia < ib);
 }

@@ -1121,6 +1121,31 @@ struct CtaMerge {
     float lane_max[NW][32];  // running lane maxima of the current row (-inf between rows)
 };
 
+// Next-token logits (one logits row per batch: output row o reads logits row o). Warp w
+// of a CTA that starts on a task of its own (blockIdx.x < min(B * S, SMs)) prefetches
+// the first kPrefetchVec vectors of its part of that task into L2, before the offsets are
+// read, so that HBM already works during that round trip. The range is computed as in
+// stream_piece and lies inside logits row o (o < B = rows of logits); the prefetch is a
+// hint and changes no result, even when the offsets turn out to be bad.
+constexpr uint32_t kPrefetchVec = 512;  // 8 KB per warp
+
+template <int NW>
+__device__ __forceinline__ void prefetch_own_task(const RowsParams& p, int w) {
+    const uint32_t S = p.split, ntask = p.B * S, nA = ntask < p.num_sms ? ntask : p.num_sms;
+    if (blockIdx.x >= nA) return;
+    const uint32_t o = blockIdx.x / S, piece = blockIdx.x - o * S;
+    const uint32_t pq0 = (uint32_t)(((uint64_t)p.nq * piece) / S);
+    const uint32_t pq1 = (uint32_t)(((uint64_t)p.nq * (piece + 1)) / S);
+    const uint32_t q0 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * w) / NW);
+    const uint32_t q1 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * (w + 1)) / NW);
+    const float* rowp = p.logits + (size_t)o * p.V;
+    const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
+    const uint32_t qf = a ? 1u : 0u, qe = (p.V + (uint32_t)a) >> 2;
+    const uint32_t qa = max(q0, qf), qb = max(min(q1, qe), qa);
+    const uint32_t n = min(qb - qa, kPrefetchVec);
+    if (n) prefetch_l2_bulk(rowp - a + 4 * (size_t)qa, 16u * n);
+}
+
 constexpr int kQueueWarps = LP_QUEUE_WARPS;
 constexpr int kQueueStages = LP_QUEUE_STAGES;
 constexpr int kQueueUnroll = LP_QUEUE_UNROLL;
@@ -1144,6 +1169,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const bool early = p.early && p.stage_offsets;
     uint32_t status, R;
     if (early) {
+        // The logits are complete (the plan, launched after all earlier work, is running).
+        if (p.T_logits == B && lane == 0) prefetch_own_task<NW>(p, w);
         // rows derived here: the plan may still be running (see RowsParams::early)
         bool bad;
         stage_and_scan<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo, R, bad);

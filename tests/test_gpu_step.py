@@ -123,3 +123,25 @@ def test_step_repeated_then_compute(kernel, monkeypatch):
     for got in (first, again):
         assert got[1] == 0
         assert np.array_equal(got[4][:40], r_tok) and np.array_equal(got[3][:40], r_lp, equal_nan=True)
+
+
+@pytest.mark.parametrize("B,V", [(200, 70001), (152, 128256), (40, 250007), (1, 33)])
+def test_step_next_token_prefetch(B, V, monkeypatch):
+    # One logits row per batch: each CTA that starts on a task of its own prefetches its
+    # warps' first blocks of that row into L2 before it reads the offsets (odd V: rows not
+    # 16-byte aligned; 40 rows: split pieces; 152 rows: one task per SM). A hint only:
+    # the rows equal plan + compute bit for bit.
+    monkeypatch.setenv("LP_RAGGED_KERNEL", "queue")
+    check_equal(workloads.make_next_token_batch(B, V, levels=3, device="cuda", seed=B), f"next-token {B}x{V}")
+
+
+def test_step_next_token_bad_offsets_write_no_row():
+    # One logits row per batch, so the prefetch guesses row o for output row o; with
+    # non-monotone offsets the guess is wrong, nothing is written and the status says so.
+    g = torch.Generator().manual_seed(17)
+    x = torch.randn(5, 70001, generator=g).cuda()
+    b = workloads.make_custom_batch(x, [1] * 5, [0] * 5, 3, seed=17)
+    b.logit_row_offsets.copy_(torch.tensor([0, 1, 3, 2, 4, 5], dtype=torch.int32))
+    R, status, _, g_lp, g_tok = run_step(b, sentinel=True)
+    assert status & BIT_OFFSETS
+    assert np.all(g_lp == 123.25) and np.all(g_tok == 77)
