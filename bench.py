@@ -66,13 +66,13 @@ def load_batch(config: str, variant: str, dev):
 # keyed by workload, valid only while the kernel sources hash to the recorded value.
 # Filled from the captures summarised under profiles/.
 NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 134618880, "source_hash": "b0e63e470d1f1323",
+    "decode": {"bytes_per_launch": 134853888, "source_hash": "6fd7066c773f5b7f",
                "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 903196416, "source_hash": "b0e63e470d1f1323",
+    "prefill": {"bytes_per_launch": 903405568, "source_hash": "6fd7066c773f5b7f",
                 "capture": "profiles/k_rows_prefill.md"},
-    "mixed": {"bytes_per_launch": 3336375040, "source_hash": "b0e63e470d1f1323",
+    "mixed": {"bytes_per_launch": 3336594432, "source_hash": "6fd7066c773f5b7f",
               "capture": "profiles/k_rows_mixed_wide_dram.md"},
-    "wide": {"bytes_per_launch": 22139949312, "source_hash": "b0e63e470d1f1323",
+    "wide": {"bytes_per_launch": 22139009280, "source_hash": "6fd7066c773f5b7f",
              "capture": "profiles/k_rows_mixed_wide_dram.md"},
 }
 

@@ -1367,8 +1367,9 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         }
     }
     if (early) pdl_wait();
+    // No fence before the count: this CTA's queue requests have all returned, and nothing
+    // it wrote is read again in this launch (the next call sees it after the kernel ends).
     if (threadIdx.x == 0) {
-        __threadfence();
         if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {  // last CTA out: ready for the next call
             queue[0] = 0u;
             queue[1] = 0u;
