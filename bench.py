@@ -113,7 +113,7 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def uses_row_queue(rows_bound: int, V: int) -> bool:
+def uses_row_queue(rows_bound: int) -> bool:
     """The library's kernel choice: the row-queue kernel when at most three rows per SM
     can come out; else the warp-range kernel."""
     import torch
@@ -488,8 +488,7 @@ def run_ours(args, rank: int, world: int, dist):
     if rec and rec.get("source_hash") == kernel_source_hash():
         traffic = rec["bytes_per_launch"]
     entry = "lp_ragged_shard_partials" if sharded else ("lp_ragged_compute_ex" if extended else "lp_ragged_compute")
-    shard_V = full_logits.shape[1]
-    kernel_name = (f"k_rows_cta ({entry}, row queue)" if uses_row_queue(min(T, T_logits), shard_V)
+    kernel_name = (f"k_rows_cta ({entry}, row queue)" if uses_row_queue(min(T, T_logits))
                    else f"k_rows ({entry}, warp ranges)")
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                 "timing": f"CUDA events around one CUDA-graph replay of {n_ev} back-to-back compute launches, same "

@@ -71,3 +71,44 @@ def test_reference_arm_json_line_on_cpu():
         assert key in line, key
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_code_only_strips_comments_keeps_strings():
+    sys.path.insert(0, ROOT)
+    import bench
+    src = 'int a = 1;  // note\n// whole line\nasm("x // y");  // z\n\n   \nfloat b;   \n'
+    assert bench._code_only(src) == 'int a = 1;\nasm("x // y");\nfloat b;'
+
+
+def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
+    # The recorded ncu traffic stays valid across comment edits and is voided by a code edit.
+    sys.path.insert(0, ROOT)
+    import glob
+    import shutil
+    import bench
+    csrc = tmp_path / "ragged_log_probs_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in glob.glob(os.path.join(ROOT, "ragged_log_probs_gb300", "csrc", "*.cuh")):
+        shutil.copy(f, csrc)
+    h0 = bench.kernel_source_hash()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_source_hash() == h0
+    target = csrc / "lp_device.cuh"
+    text = target.read_text(encoding="utf-8")
+    target.write_text(text + "\n// a comment added at the end\n", encoding="utf-8")
+    assert bench.kernel_source_hash() == h0
+    target.write_text(text + "\nconstexpr int kUnused = 1;\n", encoding="utf-8")
+    assert bench.kernel_source_hash() != h0
+
+
+def test_recorded_traffic_names_its_capture():
+    # Every recorded ncu traffic figure points at a committed profile summary that states the
+    # same device-code hash and the same bytes per launch (in MB, two decimals).
+    sys.path.insert(0, ROOT)
+    import bench
+    for name, rec in bench.NCU_TRAFFIC.items():
+        path = os.path.join(ROOT, rec["capture"])
+        assert os.path.isfile(path), name
+        text = open(path, encoding="utf-8").read()
+        assert rec["source_hash"] in text, name
+        assert f"{rec['bytes_per_launch'] / 1e6:.2f} MB" in text, name
