@@ -22,7 +22,7 @@ from .results import LogProbabilities, assemble  # noqa: F401  (host-side result
 
 __all__ = [
     "LpError", "lib_path", "load", "workspace_size", "new_workspace", "plan", "compute",
-    "compute_ex", "read_status", "ragged_log_probs", "tuple_bytes", "shard_partials", "shard_merge",
+    "compute_ex", "step", "read_status", "ragged_log_probs", "tuple_bytes", "shard_partials", "shard_merge",
     "gather_shard_tuples", "ragged_log_probs_vocab_parallel", "out_per_token", "STATUS_NAMES", "LogProbabilities", "assemble",
 ]
 
@@ -125,6 +125,23 @@ def _dev_u8(t: torch.Tensor, name: str, n: int) -> int:
     return t.data_ptr()
 
 
+def _dev_f32(t: torch.Tensor, name: str, n: Optional[int] = None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+        raise TypeError(f"{name} must be a float32 CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if n is not None and t.numel() < n:
+        raise ValueError(f"{name} needs {n} elements, has {t.numel()}")
+    return t.data_ptr()
+
+
+def _ws(workspace: torch.Tensor) -> int:
+    """Device pointer of a workspace tensor (the kernels write it: a host tensor is refused)."""
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor (see new_workspace)")
+    return workspace.data_ptr()
+
+
 def workspace_size(B: int, T: int, V: int, levels: int) -> int:
     """Bytes of scratch for one call on the current device."""
     return int(load().lp_ragged_workspace_size(B, T, V, levels))
@@ -158,7 +175,7 @@ def plan(logit_row_offsets: torch.Tensor, echo: torch.Tensor, T: int, workspace:
         hp = host_out.data_ptr()
     rc = lib.lp_ragged_plan(_dev_u32(logit_row_offsets, "logit_row_offsets", B + 1), _dev_u8(echo, "echo", B),
                             B, T, _dev_u32(output_row_offsets, "output_row_offsets", B + 1), hp,
-                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _ws(workspace), workspace.numel() * workspace.element_size(),
                             _stream_handle(stream))
     if rc:
         raise LpError(rc, "lp_ragged_plan")
@@ -183,7 +200,7 @@ def compute(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: torch
         _dev_u32(tokens, "tokens", T), _dev_u32(sampled_tokens, "sampled_tokens", B),
         _dev_u32(output_row_offsets, "output_row_offsets", B + 1), _dev_u8(echo, "echo", B), levels,
         out_logprobs.data_ptr(), _dev_u32(out_tokens, "out_tokens"),
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        _ws(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc:
         raise LpError(rc, "lp_ragged_compute")
 
@@ -222,7 +239,7 @@ def compute_ex(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: to
         _dev_u32(tokens, "tokens", T), _dev_u32(sampled_tokens, "sampled_tokens", B),
         _dev_u32(output_row_offsets, "output_row_offsets", B + 1), _dev_u8(echo, "echo", B), tp, levels,
         out_logprobs.data_ptr(), _dev_u32(out_tokens, "out_tokens"),
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        _ws(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc:
         raise LpError(rc, "lp_ragged_compute_ex")
 
@@ -269,7 +286,7 @@ def step(logits: torch.Tensor, logit_row_offsets: torch.Tensor, tokens: torch.Te
         logits.data_ptr(), T_logits, V, _dev_u32(logit_row_offsets, "logit_row_offsets", B + 1), ioff, T, B,
         _dev_u32(tokens, "tokens", T), _dev_u32(sampled_tokens, "sampled_tokens", B), _dev_u8(echo, "echo", B), tp,
         levels, _dev_u32(output_row_offsets, "output_row_offsets", B + 1), hp, out_logprobs.data_ptr(),
-        _dev_u32(out_tokens, "out_tokens"), rows, workspace.data_ptr(),
+        _dev_u32(out_tokens, "out_tokens"), rows, _ws(workspace),
         workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc:
         raise LpError(rc, "lp_ragged_step")
@@ -305,12 +322,12 @@ def shard_partials(logits: torch.Tensor, vocab_base: int, logit_row_offsets: tor
             tuples.numel() * tuples.element_size() < rows_capacity * tuple_bytes(levels):
         raise ValueError("tuples must be a contiguous CUDA buffer of rows_capacity * tuple_bytes(levels) bytes")
     ioff = 0 if input_row_offsets is None else _dev_u32(input_row_offsets, "input_row_offsets", B + 1)
-    tp = 0 if temperatures is None else temperatures.data_ptr()
+    tp = 0 if temperatures is None else _dev_f32(temperatures, "temperatures", B)
     rc = lib.lp_ragged_shard_partials(
         logits.data_ptr(), T_logits, V_shard, vocab_base, _dev_u32(logit_row_offsets, "logit_row_offsets", B + 1),
         ioff, T, B, _dev_u32(tokens, "tokens", T), _dev_u32(sampled_tokens, "sampled_tokens", B),
         _dev_u32(output_row_offsets, "output_row_offsets", B + 1), _dev_u8(echo, "echo", B), tp, levels,
-        tuples.data_ptr(), rows_capacity, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        tuples.data_ptr(), rows_capacity, _ws(workspace), workspace.numel() * workspace.element_size(),
         _stream_handle(stream))
     if rc:
         raise LpError(rc, "lp_ragged_shard_partials")
@@ -325,11 +342,12 @@ def shard_merge(tuples: torch.Tensor, P: int, rows_capacity: int, V: int, output
     if not tuples.is_cuda or not tuples.is_contiguous() or \
             tuples.numel() * tuples.element_size() < P * rows_capacity * tuple_bytes(levels):
         raise ValueError("tuples must hold P * rows_capacity row tuples")
-    tp = 0 if temperatures is None else temperatures.data_ptr()
+    tp = 0 if temperatures is None else _dev_f32(temperatures, "temperatures", B)
     rc = lib.lp_ragged_shard_merge(tuples.data_ptr(), P, rows_capacity, V,
                                    _dev_u32(output_row_offsets, "output_row_offsets", B + 1), B, tp, levels,
-                                   out_logprobs.data_ptr(), _dev_u32(out_tokens, "out_tokens"), workspace.data_ptr(),
-                                   workspace.numel() * workspace.element_size(), _stream_handle(stream))
+                                   _dev_f32(out_logprobs, "out_logprobs"), _dev_u32(out_tokens, "out_tokens"),
+                                   _ws(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream_handle(stream))
     if rc:
         raise LpError(rc, "lp_ragged_shard_merge")
 
@@ -387,8 +405,9 @@ def ragged_log_probs_vocab_parallel(logits_shard: torch.Tensor, vocab_base: int,
 def read_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronously read the device status bits (bit c set <=> error code c seen)."""
     lib = load()
+    wp = _ws(workspace)
     host = torch.zeros(1, dtype=torch.int32).pin_memory()
-    rc = lib.lp_ragged_read_status(workspace.data_ptr(), host.data_ptr(), _stream_handle(stream))
+    rc = lib.lp_ragged_read_status(wp, host.data_ptr(), _stream_handle(stream))
     if rc:
         raise LpError(rc, "lp_ragged_read_status")
     (torch.cuda.current_stream() if stream is None else stream).synchronize()

@@ -161,6 +161,21 @@ def test_package_fails_loudly_without_library(monkeypatch, tmp_path):
         lp.load()
 
 
+def test_binding_refuses_host_buffers_before_any_launch(lib):
+    # The kernels write the workspace and read every array: host tensors are refused in the
+    # binding, before a pointer reaches the library.
+    import torch
+    import ragged_log_probs_gb300 as lp
+    with pytest.raises(TypeError):
+        lp.read_status(torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(TypeError):
+        lp._dev_f32(torch.zeros(4), "temperatures")
+    with pytest.raises(TypeError):
+        lp._dev_u32(torch.zeros(4, dtype=torch.int32), "tokens")
+    with pytest.raises(TypeError):
+        lp._dev_u8(torch.zeros(4, dtype=torch.uint8), "echo", 4)
+
+
 def test_row_kernels_static_shared_memory_keeps_rings_aligned(tmp_path, capfd):
     # The rings live in dynamic shared memory, which starts where a kernel's static shared
     # memory ends: a static size off a multiple of 128 bytes would make every warp's
