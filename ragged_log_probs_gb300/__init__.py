@@ -103,9 +103,17 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream)
 
 
+def _on_current_device(t: torch.Tensor, name: str) -> None:
+    # The library launches on the current device: another GPU's pointer would reach the kernel.
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{cur}")
+
+
 def _dev_u32(t: torch.Tensor, name: str, n: Optional[int] = None) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    _on_current_device(t, name)
     if t.dtype not in (torch.int32, torch.uint32):
         raise TypeError(f"{name} must be int32/uint32, got {t.dtype}")
     if not t.is_contiguous():
@@ -118,6 +126,7 @@ def _dev_u32(t: torch.Tensor, name: str, n: Optional[int] = None) -> int:
 def _dev_u8(t: torch.Tensor, name: str, n: int) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    _on_current_device(t, name)
     if t.dtype not in (torch.uint8, torch.bool, torch.int8):
         raise TypeError(f"{name} must be uint8/bool, got {t.dtype}")
     if not t.is_contiguous() or t.numel() < n:
@@ -128,6 +137,7 @@ def _dev_u8(t: torch.Tensor, name: str, n: int) -> int:
 def _dev_f32(t: torch.Tensor, name: str, n: Optional[int] = None) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
         raise TypeError(f"{name} must be a float32 CUDA tensor")
+    _on_current_device(t, name)
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if n is not None and t.numel() < n:
@@ -139,6 +149,7 @@ def _ws(workspace: torch.Tensor) -> int:
     """Device pointer of a workspace tensor (the kernels write it: a host tensor is refused)."""
     if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
         raise TypeError("workspace must be a contiguous CUDA tensor (see new_workspace)")
+    _on_current_device(workspace, "workspace")
     return workspace.data_ptr()
 
 
