@@ -112,3 +112,12 @@ def test_recorded_traffic_names_its_capture():
         text = open(path, encoding="utf-8").read()
         assert rec["source_hash"] in text, name
         assert f"{rec['bytes_per_launch'] / 1e6:.2f} MB" in text, name
+
+
+def test_oracle_one_core_timing_on_cpu():
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    b = workloads.make_batch("tiny", "cpu")
+    k, dt = bench.time_oracle_one_core(b, budget_s=0.2, max_rows=8)
+    assert 1 <= k <= 8 and dt > 0
