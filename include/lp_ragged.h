@@ -256,15 +256,25 @@ lp_status lp_ragged_shard_merge(const void *tuples, uint32_t P, uint32_t rows_ca
  * reserved up front by its own pool and that forbids cudaMalloc on the request
  * path, where cudaMalloc may synchronise the device; or a binding with no device
  * allocator of its own).
- *   Same arguments and checks as lp_ragged_compute, minus the workspace. The
+ *   Same arguments and host checks as lp_ragged_compute, minus the workspace. The
  *   scratch is a static device array of LP_NOALLOC_SCRATCH_BYTES inside this
  *   library, held by every GPU that loads it until the process exits.
+ *   output_row_offsets  the plan's output (device, uint32[B+1]). lp_ragged_plan needs
+ *                a workspace of at least 256 + 4 x (SMs x 32) bytes rounded up to
+ *                256 (its status word and counters); a caller that has none can
+ *                compute the same values on the host (an exclusive running sum of
+ *                echo[b] ? len_b : 1) and copy them in.
  *   host_status  optional host word (pinned for an async copy): the status bits of
  *                this call, valid once the stream reaches this point; NULL skips.
+ *                They include the plan's offsets check: the call validates the
+ *                offsets itself first, and on a layout lp_ragged_plan rejects it
+ *                writes no row and sets the LP_ERR_OFFSETS bit.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
- *   capture. Each call zeroes the status word and arrival counters first, and no
- *   allocating routine (cudaMalloc, cudaFree, a library allocator) is called.
+ *   capture. Every host check runs before anything is enqueued; then the call
+ *   clears the status word and arrival counters itself (two launches: the
+ *   validation, then the reduction), and no allocating routine (cudaMalloc,
+ *   cudaFree, a library allocator) is called.
  *   Returns LP_ERR_WORKSPACE when this GPU needs more scratch than the array holds
  *   (more than ~245 SMs at levels 6). All calls share the array: calls that overlap
  *   on the GPU (other streams, other host threads) race; serialise them.

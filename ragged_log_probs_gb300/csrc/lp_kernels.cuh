@@ -20,10 +20,11 @@
 // Sum-exp in the log2 domain. A lane keeps m (largest logit seen), c = m*k rounded to
 // fp32 with k = log2(e)/tau (tau = 1 unless a temperature is given), and
 // s = sum 2^(x*k - c): one FFMA, one EX2 and one FADD per logit. A logprob is then
-// (x*k - c)*ln2 - ln(s), formed in fp64 from the same fp32 k, so it is the exact
-// log-softmax of logits scaled by (1 + d)/tau, |d| <= 2^-24 (the rounding of k): the
-// error is |d| times the logit's distance from the softmax-weighted mean, below
-// 2^-24 * |logprob|.
+// x/tau - c/(k*tau) - ln(s), formed in fp64: c/k is the reference on the logit scale
+// taken with the same fp32 k the sum used, so s = sum exp((x_i - c/k)(1 + d)/tau) with
+// |d| <= 2^-24 the rounding of k. That rounding only reweights the terms: ln(s) moves
+// by about d times the softmax-weighted mean of (x_i - c/k)/tau (a few units at most),
+// far below the fp32 sum's own rounding, and no error grows with |logprob|.
 #pragma once
 
 #include <cstdint>
@@ -64,7 +65,6 @@ constexpr int kPlanThreads = 1024;
 constexpr uint32_t kStatusOffsets = 1u << 4;     // bit of LP_ERR_OFFSETS
 constexpr uint32_t kStatusTokenRange = 1u << 5;  // bit of LP_ERR_TOKEN_RANGE
 constexpr uint32_t kStatusTemperature = 1u << 8; // bit of LP_ERR_TEMPERATURE
-constexpr double kLn2 = 0.69314718055994530942;
 
 // Workspace: [header 256 B][arrival counters u32 x max warps, zeroed by plan, padded
 // to 256 B][partial slots].
@@ -128,7 +128,8 @@ struct RowsParams {
 constexpr uint32_t kTupleHolds = 0x80000000u;
 
 // ---------------------------------------------------------------------------------
-// Plan: one CTA, chunked block-wide exclusive scan.
+// Plan: one CTA, chunked block-wide exclusive scan. With out_off == nullptr it only
+// validates the offsets, counts the rows and clears the status word and counters.
 __global__ void __launch_bounds__(kPlanThreads) k_plan(const uint32_t* __restrict__ off,
                                                        const uint8_t* __restrict__ echo, uint32_t B,
                                                        uint32_t T, uint32_t* __restrict__ out_off,
@@ -171,13 +172,13 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(const uint32_t* __restric
         }
         __syncthreads();
         const uint32_t incl = x + (w ? s_warp[w - 1] : 0u);
-        if (i < B) out_off[i] = s_carry + incl - cnt;
+        if (i < B && out_off != nullptr) out_off[i] = s_carry + incl - cnt;
         __syncthreads();
         if (tid == kPlanThreads - 1) s_carry += incl;
         __syncthreads();
     }
     if (tid == 0) {
-        out_off[B] = s_carry;
+        if (out_off != nullptr) out_off[B] = s_carry;
         hdr->rows = s_carry;
         hdr->status = s_bad ? kStatusOffsets : 0u;
     }
@@ -410,6 +411,132 @@ __device__ __forceinline__ uint32_t live_mask(uint32_t idb, uint32_t id_end) {
     return mk;
 }
 
+// Top-k work of one block (U vectors per lane) whose largest element in this lane is
+// bm: threshold refreshes on the schedule of refresh_due, then the block's elements
+// at or above the threshold go to the candidate buffer. `partial`: the block holds
+// ring padding (ids from id_end on), which must not become candidates. slot_f is
+// the block's values in shared memory (all lanes), read back by the append.
+template <int SLOTS, bool TOPK, int U, int TABW>
+__device__ __forceinline__ void select_block(const float4 (&v)[U], float bm, uint32_t blk, bool partial,
+                                             uint32_t idb, uint32_t id_end, const float* slot_f, const LaneSum& ls,
+                                             Selector<SLOTS>& sel, int lane, uint32_t* shared_thr, float* lane_tab,
+                                             int w) {
+    if constexpr (TOPK && SLOTS == 1) {
+        // The K-th largest of the 32 lanes' running maxima is the value of K distinct
+        // elements already seen, so no element below it can be in the top-k: a
+        // threshold that follows the warp's true K-th best at the cost of one float
+        // sort, refreshed on blocks 0, 1, 2 and 4 (it rises fastest early) and then
+        // every kThrEvery blocks.
+        if (refresh_due(blk)) {
+            float lm = ls.m;
+            uint32_t kk = sel.K;
+            if constexpr (TABW > 0) {
+                volatile float* tab = lane_tab;
+                tab[w * 32 + lane] = lm;
+                if (kk <= 15u || blk < kThrEvery) {
+#pragma unroll
+                    for (int j = 0; j < TABW; ++j) lm = fmaxf(lm, tab[j * 32 + lane]);
+                } else {
+                    // K = 16..31: the K-th of 32 column maxima is nearly their minimum.
+                    // Each lane position's second best across the warps instead: the
+                    // k-th largest of those stands above 2k distinct elements (the k
+                    // second bests and the k bests above them), so k = ceil(K/2). Not on
+                    // the first blocks, while few warps have published their maxima
+                    // (the second bests are then mostly -inf).
+                    float hi = neg_inf(), lo = neg_inf();
+#pragma unroll
+                    for (int j = 0; j < TABW; ++j) {
+                        const float v2 = tab[j * 32 + lane];
+                        lo = fmaxf(lo, fminf(hi, v2));
+                        hi = fmaxf(hi, v2);
+                    }
+                    lm = lo;
+                    kk = (kk + 1u) >> 1;
+                }
+            }
+            sel.thr = fmaxf(sel.thr, kth_largest32(lm, kk, lane));
+            if (shared_thr != nullptr) {  // warps on the same row share their thresholds
+                if (lane == 0 && sel.thr != neg_inf()) atomicMax(shared_thr, f2ord(sel.thr));
+                sel.thr = fmaxf(sel.thr, ord2f(*(volatile uint32_t*)shared_thr));
+            }
+        }
+        if (__any_sync(kFull, bm >= sel.thr)) {
+            uint32_t mk = block_mask<U>(v, sel.thr);
+            if (partial) mk &= live_mask<U>(idb, id_end);
+            sel.append_block(slot_f, mk, idb, lane);
+        }
+    }
+    if constexpr (TOPK && SLOTS == 2) {
+        // K = 63 > 32 lanes: a bound needs 64 distinct elements. With TABW warps on the
+        // row, each lane position takes the two best of the warps' lane maxima (elements
+        // of two different (warp, lane) streams); the 63rd largest of those 64 values
+        // (their second smallest) bounds the top-63. (Tracking a second maximum per lane
+        // in the warp-range kernel costs more than it saves.)
+        if (TABW > 0 && blk != 0 && refresh_due(blk)) {
+            float hi = neg_inf(), lo = neg_inf();
+            volatile float* tab = lane_tab;
+            tab[w * 32 + lane] = ls.m;
+#pragma unroll
+            for (int j = 0; j < TABW; ++j) {
+                const float v2 = tab[j * 32 + lane];
+                lo = fmaxf(lo, fminf(hi, v2));
+                hi = fmaxf(hi, v2);
+            }
+            // two smallest of the 64 values (lo <= hi in every lane)
+#pragma unroll
+            for (int d2 = 16; d2 > 0; d2 >>= 1) {
+                const float olo = __shfl_xor_sync(kFull, lo, d2), ohi = __shfl_xor_sync(kFull, hi, d2);
+                const float nhi = fminf(fmaxf(lo, olo), fminf(hi, ohi));
+                lo = fminf(lo, olo);
+                hi = nhi;
+            }
+            sel.thr = fmaxf(sel.thr, hi);
+            if (shared_thr != nullptr) {
+                if (lane == 0 && sel.thr != neg_inf()) atomicMax(shared_thr, f2ord(sel.thr));
+                sel.thr = fmaxf(sel.thr, ord2f(*(volatile uint32_t*)shared_thr));
+            }
+        }
+        if (blk == 0 && sel.cnt == 0 && sel.thr == neg_inf()) {
+            // Seed the list with each lane's best (and second best) element of this
+            // block, scanned in id order, so the threshold is useful at once.
+            float b1 = neg_inf(), b2 = neg_inf();
+            int p1 = -1, p2 = -1;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float x = pick(v[u], k);
+                    if (x > b1) {
+                        b2 = b1; p2 = p1;
+                        b1 = x; p1 = u * 4 + k;
+                    } else if (SLOTS == 2 && x > b2) {
+                        b2 = x; p2 = u * 4 + k;
+                    }
+                }
+            }
+            const uint32_t i1 = p1 >= 0 ? idb + 128u * (uint32_t)(p1 >> 2) + (uint32_t)(p1 & 3) : kPadId;
+            sel.L.insert32(b1, i1, lane);
+            if constexpr (SLOTS == 2) {
+                const uint32_t i2 = p2 >= 0 ? idb + 128u * (uint32_t)(p2 >> 2) + (uint32_t)(p2 & 3) : kPadId;
+                sel.L.insert32(b2, i2, lane);
+            }
+            sel.thr = sel.L.kth(sel.K);
+            if (__any_sync(kFull, bm >= sel.thr)) {
+                uint32_t ex = 0;  // the seeded elements are already in the list
+                if (p1 >= 0) ex |= 1u << p1;
+                if (SLOTS == 2 && p2 >= 0) ex |= 1u << p2;
+                uint32_t mk = block_mask<U>(v, sel.thr) & ~ex;
+                if (partial) mk &= live_mask<U>(idb, id_end);
+                sel.append_block(slot_f, mk, idb, lane);
+            }
+        } else if (__any_sync(kFull, bm >= sel.thr)) {
+            uint32_t mk = block_mask<U>(v, sel.thr);
+            if (partial) mk &= live_mask<U>(idb, id_end);
+            sel.append_block(slot_f, mk, idb, lane);
+        }
+    }
+}
+
 // Stream vectors [q0, q1) of one row: running sum per lane, top-k per warp.
 // Full blocks (U vectors per lane, 512*U contiguous bytes per warp) go through a ring
 // of STAGES blocks in shared memory filled by cp.async, so STAGES-1 blocks stay in
@@ -492,120 +619,8 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
         if ((U & 1) == 0) bm = fmaxf(bm, mu[U - 1]);
         ls.add_block<U>(v, bm);
 
-        if constexpr (TOPK && SLOTS == 1) {
-            // The K-th largest of the 32 lanes' running maxima is the value of K distinct
-            // elements already seen, so no element below it can be in the top-k: a
-            // threshold that follows the warp's true K-th best at the cost of one float
-            // sort, refreshed on blocks 0, 1, 2 and 4 (it rises fastest early) and then
-            // every kThrEvery blocks.
-            if (refresh_due(blk)) {
-                float lm = ls.m;
-                uint32_t kk = sel.K;
-                if constexpr (TABW > 0) {
-                    volatile float* tab = lane_tab;
-                    tab[w * 32 + lane] = lm;
-                    if (kk <= 15u || blk < kThrEvery) {
-#pragma unroll
-                        for (int j = 0; j < TABW; ++j) lm = fmaxf(lm, tab[j * 32 + lane]);
-                    } else {
-                        // K = 16..31: the K-th of 32 column maxima is nearly their minimum.
-                        // Each lane position's second best across the warps instead: the
-                        // k-th largest of those stands above 2k distinct elements (the k
-                        // second bests and the k bests above them), so k = ceil(K/2). Not on
-                        // the first blocks, while few warps have published their maxima
-                        // (the second bests are then mostly -inf).
-                        float hi = neg_inf(), lo = neg_inf();
-#pragma unroll
-                        for (int j = 0; j < TABW; ++j) {
-                            const float v2 = tab[j * 32 + lane];
-                            lo = fmaxf(lo, fminf(hi, v2));
-                            hi = fmaxf(hi, v2);
-                        }
-                        lm = lo;
-                        kk = (kk + 1u) >> 1;
-                    }
-                }
-                sel.thr = fmaxf(sel.thr, kth_largest32(lm, kk, lane));
-                if (shared_thr != nullptr) {  // warps on the same row share their thresholds
-                    if (lane == 0 && sel.thr != neg_inf()) atomicMax(shared_thr, f2ord(sel.thr));
-                    sel.thr = fmaxf(sel.thr, ord2f(*(volatile uint32_t*)shared_thr));
-                }
-            }
-            if (__any_sync(kFull, bm >= sel.thr)) {
-                uint32_t mk = block_mask<U>(v, sel.thr);
-                if (blk + 1u == nblk && rem != 0u) mk &= live_mask<U>(idb, id_end);
-                sel.append_block(slot_f, mk, idb, lane);
-            }
-        }
-        if constexpr (TOPK && SLOTS == 2) {
-            // K = 63 > 32 lanes: a bound needs 64 distinct elements. With TABW warps on the
-            // row, each lane position takes the two best of the warps' lane maxima (elements
-            // of two different (warp, lane) streams); the 63rd largest of those 64 values
-            // (their second smallest) bounds the top-63. (Tracking a second maximum per lane
-            // in the warp-range kernel costs more than it saves.)
-            if (TABW > 0 && blk != 0 && refresh_due(blk)) {
-                float hi = neg_inf(), lo = neg_inf();
-                volatile float* tab = lane_tab;
-                tab[w * 32 + lane] = ls.m;
-#pragma unroll
-                for (int j = 0; j < TABW; ++j) {
-                    const float v2 = tab[j * 32 + lane];
-                    lo = fmaxf(lo, fminf(hi, v2));
-                    hi = fmaxf(hi, v2);
-                }
-                // two smallest of the 64 values (lo <= hi in every lane)
-#pragma unroll
-                for (int d2 = 16; d2 > 0; d2 >>= 1) {
-                    const float olo = __shfl_xor_sync(kFull, lo, d2), ohi = __shfl_xor_sync(kFull, hi, d2);
-                    const float nhi = fminf(fmaxf(lo, olo), fminf(hi, ohi));
-                    lo = fminf(lo, olo);
-                    hi = nhi;
-                }
-                sel.thr = fmaxf(sel.thr, hi);
-                if (shared_thr != nullptr) {
-                    if (lane == 0 && sel.thr != neg_inf()) atomicMax(shared_thr, f2ord(sel.thr));
-                    sel.thr = fmaxf(sel.thr, ord2f(*(volatile uint32_t*)shared_thr));
-                }
-            }
-            if (blk == 0 && sel.cnt == 0 && sel.thr == neg_inf()) {
-                // Seed the list with each lane's best (and second best) element of this
-                // block, scanned in id order, so the threshold is useful at once.
-                float b1 = neg_inf(), b2 = neg_inf();
-                int p1 = -1, p2 = -1;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float x = pick(v[u], k);
-                        if (x > b1) {
-                            b2 = b1; p2 = p1;
-                            b1 = x; p1 = u * 4 + k;
-                        } else if (SLOTS == 2 && x > b2) {
-                            b2 = x; p2 = u * 4 + k;
-                        }
-                    }
-                }
-                const uint32_t i1 = p1 >= 0 ? idb + 128u * (uint32_t)(p1 >> 2) + (uint32_t)(p1 & 3) : kPadId;
-                sel.L.insert32(b1, i1, lane);
-                if constexpr (SLOTS == 2) {
-                    const uint32_t i2 = p2 >= 0 ? idb + 128u * (uint32_t)(p2 >> 2) + (uint32_t)(p2 & 3) : kPadId;
-                    sel.L.insert32(b2, i2, lane);
-                }
-                sel.thr = sel.L.kth(sel.K);
-                if (__any_sync(kFull, bm >= sel.thr)) {
-                    uint32_t ex = 0;  // the seeded elements are already in the list
-                    if (p1 >= 0) ex |= 1u << p1;
-                    if (SLOTS == 2 && p2 >= 0) ex |= 1u << p2;
-                    uint32_t mk = block_mask<U>(v, sel.thr) & ~ex;
-                    if (blk + 1u == nblk && rem != 0u) mk &= live_mask<U>(idb, id_end);
-                    sel.append_block(slot_f, mk, idb, lane);
-                }
-            } else if (__any_sync(kFull, bm >= sel.thr)) {
-                uint32_t mk = block_mask<U>(v, sel.thr);
-                if (blk + 1u == nblk && rem != 0u) mk &= live_mask<U>(idb, id_end);
-                sel.append_block(slot_f, mk, idb, lane);
-            }
-        }
+        select_block<SLOTS, TOPK, U, TABW>(v, bm, blk, blk + 1u == nblk && rem != 0u, idb, id_end, slot_f, ls, sel,
+                                           lane, shared_thr, lane_tab, w);
         idb += 128u * U;
     }
     if (xt_pending && lane == 0) xt = rowp[t];
@@ -638,27 +653,33 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     if (ls.m != neg_inf()) ls.rebase(ls.m);
 }
 
+// 1 / fp32(log2(e)): the reference's scale factor of the plain path (tau = 1).
+constexpr double kInvLog2eF = 1.0 / (double)kLog2e;
+
 // Write one finished row: K top columns and the target column. (C, S) are the row's
-// reference and sum in the log2 domain of scale kk = log2(e)/tau; a logprob is
-// (x*kk - C)*ln2 - ln(S), formed in fp64.
+// reference and sum in the log2 domain of scale kk = fp32(log2(e)/tau); a logprob is
+// x/tau - (C/(kk*tau) + ln(S)), formed in fp64 (see the sum-exp note at the top).
 template <int SLOTS, bool TOPK>
 __device__ __forceinline__ void write_row(const RowsParams& p, uint32_t o, const WarpList<SLOTS>& L, float C,
-                                          float S, uint32_t t, bool has_xt, float xt, float kk, int lane) {
-    const double ln_s = (double)logf(S), kd = (double)kk, cd = (double)C;
+                                          float S, uint32_t t, bool has_xt, float xt, float kk, float tau,
+                                          int lane) {
+    const bool unit = tau == 1.f && kk == kLog2e;
+    const double inv_tau = unit ? 1.0 : 1.0 / (double)tau;
+    const double lse = (unit ? (double)C * kInvLog2eF : (double)C / ((double)kk * (double)tau)) + (double)logf(S);
     const size_t ro = (size_t)o * p.W;
     if constexpr (TOPK) {
 #pragma unroll
         for (int k = 0; k < SLOTS; ++k) {
             const uint32_t i = (uint32_t)lane + 32u * k;
             if (i < p.K) {
-                p.out_lp[ro + i] = (float)(((double)L.x[k] * kd - cd) * kLn2 - ln_s);
+                p.out_lp[ro + i] = (float)((double)L.x[k] * inv_tau - lse);
                 p.out_tok[ro + i] = L.id[k];
             }
         }
     }
     if (lane == 0) {
         float lpt = __int_as_float(0x7fc00000);
-        if (t < p.V && has_xt) lpt = (float)(((double)xt * kd - cd) * kLn2 - ln_s);
+        if (t < p.V && has_xt) lpt = (float)((double)xt * inv_tau - lse);
         if (t >= p.V) atomicOr(p.status, kStatusTokenRange);
         p.out_lp[ro + p.K] = lpt;
         p.out_tok[ro + p.K] = t;
@@ -840,6 +861,7 @@ struct RowDesc {
     const float* rowp;  // logits row
     uint32_t t;         // target token
     float k;            // log2(e) / tau, rounded to fp32
+    float tau;          // the batch's temperature (1 without temperatures)
     uint32_t err;       // status bit, 0 if the row is valid
 };
 
@@ -856,9 +878,11 @@ __device__ __forceinline__ RowDesc describe_row(const RowsParams& p, const uint3
                            (!EXT || ((le >= lb) && (le - lb >= cnt) && (le <= p.T_logits)));
     // tau must be positive and finite (NaN fails the first test) with log2(e)/tau finite
     d.k = kLog2e;
+    d.tau = 1.f;
     bool tau_ok = true;
     if (EXT && p.tau != nullptr) {
         const float tau = p.tau[b];
+        d.tau = tau;
         d.k = __fdiv_rn(kLog2e, tau);  // fp32: its rounding is covered by the logprob form
         tau_ok = tau > 0.f && tau <= 3.4028234663852886e38f && d.k <= 3.4028234663852886e38f;
     }
@@ -1082,7 +1106,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
                 if (EXT && p.tuple_out != nullptr)
                     store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, S, t, has_xt, xt_row, lane);
                 else
-                    write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, has_xt, xt_row, d.k, lane);
+                    write_row<SLOTS, TOPK>(p, o, sel.L, C, S, t, has_xt, xt_row, d.k, d.tau, lane);
             }
         }
 
@@ -1300,7 +1324,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                 if (EXT && p.tuple_out != nullptr)
                     store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, lane);
                 else
-                    write_row<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, d.k, lane);
+                    write_row<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, d.k, d.tau, lane);
             } else {
                 // a piece of a split row: publish it; the CTA that takes the row's last
                 // ticket merges all pieces
@@ -1356,7 +1380,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                 if (EXT && p.tuple_out != nullptr)
                     store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, lane);
                 else
-                    write_row<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, d.k, lane);
+                    write_row<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, d.k, d.tau, lane);
                 __syncwarp();
                 if (lane == 0) {
                     tickets[o] = 0u;  // ready for the next call
@@ -1447,16 +1471,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32) k_shard_merge(RowsParams p, 
                     if (j0 + q < P) merge_lists<SLOTS>(L.x, L.id, bx[q], bi[q], lane);
             }
         }
-        float kk = kLog2e;
+        float kk = kLog2e, tau = 1.f;
         if (p.tau != nullptr) {  // same scale as the shards used (validated there)
             uint32_t lo = 0, hi = p.B;
             while (hi - lo > 1) {
                 const uint32_t mid = (lo + hi) >> 1;
                 if (__ldg(p.out_off + mid) <= o) lo = mid; else hi = mid;
             }
-            kk = __fdiv_rn(kLog2e, __ldg(p.tau + lo));
+            tau = __ldg(p.tau + lo);
+            kk = __fdiv_rn(kLog2e, tau);
         }
-        write_row<SLOTS, TOPK>(p, o, L, C, S, t, has_xt, xt, kk, lane);
+        write_row<SLOTS, TOPK>(p, o, L, C, S, t, has_xt, xt, kk, tau, lane);
     }
 }
 

@@ -141,11 +141,13 @@ size_t lp_ragged_workspace_size(uint32_t B, uint32_t T, uint32_t V, uint32_t lev
 
 }  // extern "C"
 
-// The plan kernel's launch (lp_ragged_plan without the host copy).
+// The plan kernel's launch (lp_ragged_plan without the host copy). With
+// validate_only the kernel writes no output offsets (output_row_offsets may be NULL):
+// it checks the offsets, counts the rows and clears the status word and counters.
 static lp_status plan_launch(const uint32_t* logit_row_offsets, const uint8_t* echo, uint32_t B, uint32_t T,
                              uint32_t* output_row_offsets, void* workspace, size_t workspace_bytes,
-                             cudaStream_t s) {
-    if (!logit_row_offsets || !echo || !output_row_offsets) return LP_ERR_NULL;
+                             cudaStream_t s, bool validate_only = false) {
+    if (!logit_row_offsets || !echo || (!output_row_offsets && !validate_only)) return LP_ERR_NULL;
     if (!workspace) return LP_ERR_WORKSPACE;
     if (B == 0 || T == 0) return LP_ERR_SHAPE;
     if (((uintptr_t)workspace & 255u) != 0) return LP_ERR_WORKSPACE;
@@ -156,8 +158,8 @@ static lp_status plan_launch(const uint32_t* logit_row_offsets, const uint8_t* e
     if (workspace_bytes < sizeof(lpk::WsHeader) + counters_bytes(g_max)) return LP_ERR_WORKSPACE;
     auto* hdr = static_cast<lpk::WsHeader*>(workspace);
     auto* counters = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) + sizeof(lpk::WsHeader));
-    lpk::k_plan<<<1, lpk::kPlanThreads, 0, s>>>(logit_row_offsets, echo, B, T, output_row_offsets, hdr, counters,
-                                               g_max);
+    lpk::k_plan<<<1, lpk::kPlanThreads, 0, s>>>(logit_row_offsets, echo, B, T,
+                                               validate_only ? nullptr : output_row_offsets, hdr, counters, g_max);
     if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
     return LP_OK;
 }
@@ -460,14 +462,14 @@ const char* lp_ragged_strerror(lp_status status) {
 // ---------------------------------------------------------------------------------
 // Allocation-free variant of lp_ragged_compute.
 //
-// Its scratch (status word, arrival counters, split-row partial tuples)
-// lives in one file-scope device array instead of a caller-provided workspace.
-// Every GPU that loads this library holds the array until the process exits; all
-// calls on a device share it, so calls that overlap on the GPU (two streams, two
-// threads) race and corrupt each other's results.
-namespace {
+// Its scratch (status word, arrival counters, split-row partial tuples) lives in one
+// file-scope device array instead of a caller-provided workspace. Every GPU that loads
+// this library holds the array until the process exits; all calls on a device share
+// it, so calls that overlap on the GPU (two streams, two threads) race and corrupt each
+// other's results.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LP_NOALLOC_SCRATCH_BYTES];
 
-__device__ __align__(256) unsigned char g_noalloc_scratch[LP_NOALLOC_SCRATCH_BYTES];
+namespace {
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kMaxDevices] = {};
@@ -508,17 +510,22 @@ extern "C" lp_status lp_ragged_compute_noalloc(const float* logits, uint32_t T, 
     if (need > (size_t)LP_NOALLOC_SCRATCH_BYTES) return LP_ERR_WORKSPACE;  // GPU has too many SMs for it
     void* scratch = nullptr;
     if (!noalloc_scratch(dev, &scratch)) return LP_ERR_CUDA;
-    // The array keeps the previous call's contents: zero the status word and the
-    // arrival counters (the partial tuples are always written before they are read).
-    const uint32_t g_max = max_warps(d->sms);
+    // Every host check before anything is enqueued: a call that fails one leaves the
+    // shared array untouched (another call may still be using it).
+    const lp_status chk = compute_checks(logits, T, V, logit_row_offsets, nullptr, T, B, tokens, sampled_tokens,
+                                         output_row_offsets, echo, levels, out_logprobs, out_tokens, nullptr,
+                                         scratch, LP_NOALLOC_SCRATCH_BYTES, &d);
+    if (chk != LP_OK) return chk;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, sizeof(lpk::WsHeader) + counters_bytes(g_max), s) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return LP_ERR_CUDA;
-    }
-    const lp_status st = lp_ragged_compute(logits, T, V, logit_row_offsets, B, tokens, sampled_tokens,
-                                           output_row_offsets, echo, levels, out_logprobs, out_tokens, scratch,
-                                           LP_NOALLOC_SCRATCH_BYTES, stream);
+    // The array keeps the previous call's contents. The plan kernel, run here to validate
+    // only (it writes no output offsets), clears the status word and the arrival counters
+    // and sets the offsets bit for a layout lp_ragged_plan rejects, in which case the
+    // reduction writes no row, as lp_ragged_compute does after lp_ragged_plan. (The
+    // partial tuples are always written before they are read.)
+    lp_status st = plan_launch(logit_row_offsets, echo, B, T, nullptr, scratch, LP_NOALLOC_SCRATCH_BYTES, s, true);
+    if (st != LP_OK) return st;
+    st = lp_ragged_compute(logits, T, V, logit_row_offsets, B, tokens, sampled_tokens, output_row_offsets, echo,
+                           levels, out_logprobs, out_tokens, scratch, LP_NOALLOC_SCRATCH_BYTES, stream);
     if (st != LP_OK) return st;
     if (host_status) {
         if (cudaMemcpyAsync(host_status, &static_cast<lpk::WsHeader*>(scratch)->status, 4, cudaMemcpyDeviceToHost,

@@ -1,19 +1,34 @@
-"""CUDA path vs the fp64 oracle on the five workloads (shrunk: every output row;
-full size: sampled rows) and on the FlashInfer sampling-test shape grid."""
+"""CUDA path vs the fp64 oracle on the five workloads (every output row, at full size
+and shrunk) and on the FlashInfer sampling-test shape grid."""
+
+import warnings
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
-from tests import parity
+from tests import oracle_pool, parity
 
 pytestmark = pytest.mark.gpu
+
+
+class ParityReport(UserWarning):
+    """A full-size comparison's summary, shown in pytest's warnings summary."""
 
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     parity.ensure_built()
+
+
+@pytest.fixture(scope="module")
+def pool():
+    p = oracle_pool.new_pool()
+    yield p
+    p.terminate()
+    p.join()
 
 
 def test_tiny_full():
@@ -28,17 +43,33 @@ def test_tiny_full():
     ("decode", dict()),
 ])
 def test_workload_shrunk_every_row(name, kw):
+    # decode with no overrides is the full-size decode workload
     b = workloads.make_batch(name, "cuda", **kw)
-    parity.check_batch(b)
+    err = parity.check_batch(b)
+    if not kw:
+        warnings.warn(ParityReport(f"{name} at full size: all rows match the oracle (ids exact), "
+                                   f"max |dlogprob| = {err:.3e}"))
 
 
-@pytest.mark.parametrize("name,n", [("prefill", 40), ("mixed", 40), ("wide", 24)])
-def test_workload_full_size_sampled_rows(name, n):
+@pytest.mark.parametrize("name", ["prefill", "mixed", "wide"])
+def test_workload_full_size_every_row(name, pool):
+    # The three large workloads at full size (the tiny and decode ones run whole above):
+    # every output row against the oracle, run on all host cores.
     b = workloads.make_batch(name, "cuda")
-    off, _, _, echo = b.host()
-    R = int(sum((off[i + 1] - off[i]) if echo[i] else 1 for i in range(b.B)))
-    rows = parity.sample_rows(R, n, seed=11)
-    parity.check_batch(b, rows=rows, full_copy=False)
+    g_off, g_lp, g_tok = parity.run_gpu(b)
+    off, tokens, sampled, echo = b.host()
+    ioff, tau = b.host_variant()
+    mapping = oracle.output_rows(off, echo, tokens, sampled, input_row_offsets=ioff)
+    assert np.array_equal(g_off, oracle.output_row_offsets(off if ioff is None else ioff, echo)), name
+
+    def fetch(rows):
+        idx = torch.as_tensor(rows, dtype=torch.long, device=b.logits.device)
+        return b.logits.index_select(0, idx).cpu().numpy()
+
+    r_lp, r_tok = oracle_pool.score_all_rows(pool, fetch, mapping, b.V, b.levels, taus=tau)
+    err = parity.compare(g_lp, g_tok, r_lp, r_tok, f"{name} full size, every row")
+    warnings.warn(ParityReport(f"{name} at full size: all {len(mapping)} rows x {g_lp.shape[1]} columns match "
+                               f"the oracle (ids exact), max |dlogprob| = {err:.3e}"))
     del b
     torch.cuda.empty_cache()
 
