@@ -52,6 +52,9 @@ VARIANT_TEXT = {
               "+ merge of the 8 gathered tuple slices (the all-gather between GPUs is not in the step)",
 }
 SHARDS = 8
+# Workloads timed beside the headline one in the same run (per_config), and their steps.
+PER_CONFIG = ("decode", "prefill", "mixed", "wide")
+PER_CONFIG_STEPS = 200
 
 
 def load_batch(config: str, variant: str, dev):
@@ -63,18 +66,8 @@ def load_batch(config: str, variant: str, dev):
 
 
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the row kernel,
-# keyed by workload, valid only while the kernel sources hash to the recorded value.
-# Filled from the captures summarised under profiles/.
-NCU_TRAFFIC = {
-    "decode": {"bytes_per_launch": 134853888, "source_hash": "6fd7066c773f5b7f",
-               "capture": "profiles/k_rows_cta_decode.md"},
-    "prefill": {"bytes_per_launch": 903405568, "source_hash": "6fd7066c773f5b7f",
-                "capture": "profiles/k_rows_prefill.md"},
-    "mixed": {"bytes_per_launch": 3336594432, "source_hash": "6fd7066c773f5b7f",
-              "capture": "profiles/k_rows_mixed_wide_dram.md"},
-    "wide": {"bytes_per_launch": 22139009280, "source_hash": "6fd7066c773f5b7f",
-             "capture": "profiles/k_rows_mixed_wide_dram.md"},
-}
+# keyed by workload, valid only while the kernels' device code hashes to the recorded value.
+NCU_TRAFFIC = {}
 
 
 def _code_only(text: str) -> str:
@@ -113,7 +106,7 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def uses_row_queue(rows_bound: int) -> bool:
+def few_rows(rows_bound: int) -> bool:
     """The library's kernel choice: the row-queue kernel when at most three rows per SM
     can come out; else the warp-range kernel."""
     import torch
@@ -167,6 +160,8 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
             self.out.close()
+        if self.path and os.path.exists(self.path):
+            os.unlink(self.path)
 
     def summary(self, t0: float, t1: float):
         if self.proc is None or not self.path:
@@ -182,7 +177,6 @@ class ClockSampler:
                 rows.append((ts, float(parts[3]), float(parts[4]), parts[7:11]))
             except Exception:
                 continue
-        os.unlink(self.path)
         inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
         window = "timed region"
         if not inside and rows:
@@ -277,164 +271,221 @@ def time_oracle_one_core(batch, budget_s: float = 2.0, max_rows: int = 64):
 
 
 # -------------------------------------------------------------------------- our arm
+class Workload:
+    """One workload on this rank's GPU, ready to time: its inputs (logits rotating over
+    enough copies that each step reads HBM), workspace, outputs, and the library calls of
+    one step and of one compute launch."""
+
+    def __init__(self, config: str, variant: str, dev):
+        import torch
+
+        import ragged_log_probs_gb300 as lp
+        self.lp, self.dev, self.config, self.variant = lp, dev, config, variant
+        batch = self.batch = load_batch(config, variant, dev)
+        self.B, self.T_logits, self.V, self.levels = batch.B, batch.T, batch.V, batch.levels
+        self.T = batch.tokens.numel()  # input positions (== T_logits unless VARIABLE logits)
+        self.extended = variant in ("temperature", "variable")
+        self.sharded = variant == "vocab8"
+        self.W = lp.out_per_token(self.levels)
+        self.ws = lp.new_workspace(self.B, self.T, self.V, self.levels, dev)
+        host = torch.zeros(2, dtype=torch.int32).pin_memory()
+        self.out_off = lp.plan(batch.positions_offsets, batch.echo, self.T, self.ws, host_out=host)
+        torch.cuda.synchronize()
+        self.R = int(host[0])
+        if int(host[1]) != 0:
+            raise RuntimeError(f"plan status {int(host[1])}")
+        self.out_lp = torch.empty((self.R, self.W), dtype=torch.float32, device=dev)
+        self.out_tok = torch.empty((self.R, self.W), dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+        self.full_logits = batch.logits
+        if self.sharded:
+            # Rank 0's columns; the gathered buffer holds every shard's tuples (filled once,
+            # as the all-gather would), so the merge in each step reads all P slices.
+            bounds = [round(i * self.V / SHARDS) for i in range(SHARDS + 1)]
+            stride = lp.tuple_bytes(self.levels)
+            self.gathered = torch.zeros((SHARDS, self.R * stride), dtype=torch.uint8, device=dev)
+            for p_ in range(SHARDS):
+                lp.shard_partials(batch.logits[:, bounds[p_]:bounds[p_ + 1]].contiguous(), bounds[p_],
+                                  batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, self.out_off,
+                                  batch.echo, self.levels, self.gathered[p_], self.R, self.ws)
+            self.full_logits = batch.logits[:, bounds[0]:bounds[1]].contiguous()
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = int(getattr(props, "L2_cache_size", 0) or (128 << 20))
+        self.lbytes = self.full_logits.numel() * 4
+        self.n_copies = max(1, math.ceil(3 * self.l2 / self.lbytes))
+        self.copies = [self.full_logits] + [self.full_logits.clone() for _ in range(self.n_copies - 1)]
+
+    def launch_compute(self, logits, loff, ioff, tokens, sampled, echo, tau, st=None):
+        lp, st = self.lp, (self.stream if st is None else st)
+        if self.sharded:
+            lp.shard_partials(logits, 0, loff, tokens, sampled, self.out_off, echo, self.levels, self.gathered[0],
+                              self.R, self.ws, stream=st)
+        elif self.extended:
+            lp.compute_ex(logits, loff, tokens, sampled, self.out_off, echo, self.levels, self.out_lp, self.out_tok,
+                          self.ws, input_row_offsets=ioff, temperatures=tau, stream=st)
+        else:
+            lp.compute(logits, loff, tokens, sampled, self.out_off, echo, self.levels, self.out_lp, self.out_tok,
+                       self.ws, stream=st)
+
+    def compute_k(self, k, st=None):
+        b = self.batch
+        self.launch_compute(self.copies[k % self.n_copies], b.logit_row_offsets, b.input_row_offsets, b.tokens,
+                            b.sampled_tokens, b.echo, b.temperatures, st)
+
+    def step(self, i, st=None):
+        lp, b, st = self.lp, self.batch, (self.stream if st is None else st)
+        if self.sharded:
+            lp.plan(b.positions_offsets, b.echo, self.T, self.ws, output_row_offsets=self.out_off, stream=st)
+            self.compute_k(i, st)
+            lp.shard_merge(self.gathered, SHARDS, self.R, self.V, self.out_off, self.levels, self.out_lp,
+                           self.out_tok, self.ws, stream=st)
+        else:  # plan + reduction in one call (lp_ragged_step)
+            lp.step(self.copies[i % self.n_copies], b.logit_row_offsets, b.tokens, b.sampled_tokens, b.echo,
+                    self.levels, self.out_off, self.out_lp, self.out_tok, self.ws,
+                    input_row_offsets=b.input_row_offsets, temperatures=b.temperatures, stream=st)
+
+    def capture(self, n, body):
+        """n calls of body(k, stream) captured in one CUDA graph (launch-bound loops replay
+        without host launch overhead; the library's launches carry their programmatic
+        dependencies into the graph)."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device=self.dev)
+        cs.wait_stream(self.stream)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(g, stream=cs):
+                for k in range(n):
+                    body(k, cs)
+        self.stream.wait_stream(cs)
+        return g
+
+    def warm(self, warmup: int):
+        """Eager warm-up steps (they also do the library's one-time setup) and the sanity
+        gate (parity itself is the tests' job): ids in range, logprobs <= 0."""
+        import numpy as np
+        import torch
+        for i in range(warmup):
+            self.step(i)
+        torch.cuda.synchronize()
+        if self.lp.read_status(self.ws) != 0:
+            raise RuntimeError(f"{self.config}: device status set during warm-up")
+        tok_np = self.out_tok.cpu().numpy().view(np.uint32)
+        lp_np = self.out_lp.cpu().numpy()
+        K = self.W - 1
+        if np.any(tok_np[:, :K] >= self.V) or np.any(lp_np[~np.isnan(lp_np)] > 1e-4):
+            raise RuntimeError(f"{self.config}: output sanity check failed")
+
+    def graphs(self, steps: int, n_ev: int):
+        """The timed K steps (plan + compute, inputs rotating) and, for the kernel's own
+        duration, n_ev compute launches alone, each captured once in a CUDA graph."""
+        import torch
+        self.steps, self.n_ev = steps, n_ev
+        self.g_steps = self.capture(steps, lambda k, st: self.step(k, st))
+        self.g_compute = self.capture(n_ev, lambda k, st: self.compute_k(k, st))
+        self.g_steps.replay()
+        self.g_compute.replay()
+        torch.cuda.synchronize()
+        if self.lp.read_status(self.ws) != 0:
+            raise RuntimeError(f"{self.config}: device status set during the graph warm-up")
+
+    def time_graph(self, g, n, dist=None):
+        """CUDA events on the launching stream around one replay, synchronised (and with a
+        barrier under torchrun) on both sides; returns (ms per call, wall start, wall end)."""
+        import torch
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        w0 = time.time()
+        a.record(self.stream)
+        g.replay()
+        b.record(self.stream)
+        torch.cuda.synchronize()
+        w1 = time.time()
+        if dist is not None:
+            dist.barrier()
+        return a.elapsed_time(b) / n, w0, w1
+
+    def algorithmic_bytes(self):
+        if self.sharded:  # the partial kernel: its columns read once, one tuple written per row
+            return (self.R * self.full_logits.shape[1] * 4 + self.R * self.lp.tuple_bytes(self.levels)
+                    + (self.B + 1) * 8 + self.R * 4)
+        return algorithmic_bytes(self.R, self.V, self.W, self.B)
+
+    def roofline(self, compute_ms: float) -> dict:
+        alg = self.algorithmic_bytes()
+        achieved = alg / (compute_ms / 1e3) / 1e9
+        peak, peak_src = measured_peak_hbm()
+        traffic = None
+        rec = NCU_TRAFFIC.get(self.config if self.variant == "none" else f"{self.config}/{self.variant}")
+        if rec and rec.get("source_hash") == kernel_source_hash():
+            traffic = rec["bytes_per_launch"]
+        entry = ("lp_ragged_shard_partials" if self.sharded else
+                 ("lp_ragged_compute_ex" if self.extended else "lp_ragged_compute"))
+        forced = os.environ.get("LP_RAGGED_KERNEL")
+        if forced in ("warp", "queue", "span"):
+            kind = forced
+        else:
+            kind = "queue" if few_rows(min(self.T, self.T_logits)) else "warp"
+        kernel_name = {"warp": f"k_rows ({entry}, warp ranges)", "queue": f"k_rows_cta ({entry}, row queue)",
+                       "span": f"k_rows_span ({entry}, balanced spans)"}[kind]
+        return {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
+                "timing": f"CUDA events around one CUDA-graph replay of {self.n_ev} back-to-back compute launches, "
+                          f"same stream, right after the timed steps",
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
+                "compute_ms_per_launch": round(compute_ms, 5)}
+
+    def l2_note(self) -> str:
+        return (f"inputs larger than L2: {self.n_copies} rotating logits copies of {self.lbytes / 1e6:.0f} MB "
+                f"(L2 {self.l2 / 1e6:.0f} MB)")
+
+
+def gpu_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
 def run_ours(args, rank: int, world: int, dist):
-    import numpy as np
     import torch
 
     import ragged_log_probs_gb300 as lp
-    import workloads
     from ragged_log_probs_gb300 import _build
 
     _build.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    batch = load_batch(args.config, args.variant, dev)
-    B, T_logits, V, levels = batch.B, batch.T, batch.V, batch.levels
-    T = batch.tokens.numel()  # input positions (== T_logits unless VARIABLE logits)
-    pos_off = batch.positions_offsets
-    extended = args.variant in ("temperature", "variable")
-    sharded = args.variant == "vocab8"
-    W = lp.out_per_token(levels)
-    ws = lp.new_workspace(B, T, V, levels, dev)
-    host = torch.zeros(2, dtype=torch.int32).pin_memory()
-    out_off = lp.plan(pos_off, batch.echo, T, ws, host_out=host)
-    torch.cuda.synchronize()
-    R = int(host[0])
-    if int(host[1]) != 0:
-        raise RuntimeError(f"plan status {int(host[1])}")
-    out_lp = torch.empty((R, W), dtype=torch.float32, device=dev)
-    out_tok = torch.empty((R, W), dtype=torch.int32, device=dev)
-
-    stream = torch.cuda.current_stream()
-    full_logits = batch.logits
-    if sharded:
-        # Rank 0's columns; the gathered buffer holds every shard's tuples (filled once,
-        # as the all-gather would), so the merge in each step reads all P slices.
-        bounds = [round(i * V / SHARDS) for i in range(SHARDS + 1)]
-        stride = lp.tuple_bytes(levels)
-        gathered = torch.zeros((SHARDS, R * stride), dtype=torch.uint8, device=dev)
-        for p_ in range(SHARDS):
-            lp.shard_partials(batch.logits[:, bounds[p_]:bounds[p_ + 1]].contiguous(), bounds[p_],
-                              batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, out_off, batch.echo,
-                              levels, gathered[p_], R, ws)
-        full_logits = batch.logits[:, bounds[0]:bounds[1]].contiguous()
-
-    # Rotate over enough logits copies that each step reads HBM, not L2.
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 0) or (128 << 20))
-    lbytes = full_logits.numel() * 4
-    n_copies = max(1, math.ceil(3 * l2 / lbytes))
-    copies = [full_logits] + [full_logits.clone() for _ in range(n_copies - 1)]
-
-    def launch_compute(logits, loff, ioff, tokens, sampled, echo, tau, st=None):
-        st = stream if st is None else st
-        if sharded:
-            lp.shard_partials(logits, 0, loff, tokens, sampled, out_off, echo, levels, gathered[0], R, ws,
-                              stream=st)
-        elif extended:
-            lp.compute_ex(logits, loff, tokens, sampled, out_off, echo, levels, out_lp, out_tok, ws,
-                          input_row_offsets=ioff, temperatures=tau, stream=st)
-        else:
-            lp.compute(logits, loff, tokens, sampled, out_off, echo, levels, out_lp, out_tok, ws, stream=st)
-
-    def step(i, st=None):
-        st = stream if st is None else st
-        if sharded:
-            lp.plan(pos_off, batch.echo, T, ws, output_row_offsets=out_off, stream=st)
-            launch_compute(copies[i % n_copies], batch.logit_row_offsets, batch.input_row_offsets, batch.tokens,
-                           batch.sampled_tokens, batch.echo, batch.temperatures, st)
-            lp.shard_merge(gathered, SHARDS, R, V, out_off, levels, out_lp, out_tok, ws, stream=st)
-        else:  # plan + reduction in one call (lp_ragged_step)
-            lp.step(copies[i % n_copies], batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, batch.echo,
-                    levels, out_off, out_lp, out_tok, ws, input_row_offsets=batch.input_row_offsets,
-                    temperatures=batch.temperatures, stream=st)
-
-    def capture(n, body):
-        """n calls of body(k, stream) captured in one CUDA graph (launch-bound loops replay
-        without host launch overhead; the library's launches carry their programmatic
-        dependencies into the graph)."""
-        g = torch.cuda.CUDAGraph()
-        cs = torch.cuda.Stream(device=dev)
-        cs.wait_stream(stream)
-        with torch.cuda.stream(cs):
-            with torch.cuda.graph(g, stream=cs):
-                for k in range(n):
-                    body(k, cs)
-        stream.wait_stream(cs)
-        return g
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if lp.read_status(ws) != 0:
-        raise RuntimeError("device status set during warm-up")
-
-    # Sanity gate (parity itself is the tests' job): ids in range, logprobs <= 0.
-    tok_np = out_tok.cpu().numpy().view(np.uint32)
-    lp_np = out_lp.cpu().numpy()
-    K = W - 1
-    if np.any(tok_np[:, :K] >= V) or np.any(lp_np[~np.isnan(lp_np)] > 1e-4):
-        raise RuntimeError("output sanity check failed")
-
-    uuid = None
-    try:
-        u = str(props.uuid)
-        uuid = u if u.startswith("GPU-") else "GPU-" + u
-    except Exception:
-        pass
-    # The timed K steps (plan + compute, inputs rotating) and, for the kernel's own
-    # duration, n_ev compute launches alone, each captured once in a CUDA graph (after the
-    # eager warm-up above, which also did the library's one-time setup).
-    g_steps = capture(args.steps, lambda k, st: step(k, st))
+    wl = Workload(args.config, args.variant, dev)
+    batch, B, T, T_logits, V, levels, W, R = wl.batch, wl.B, wl.T, wl.T_logits, wl.V, wl.levels, wl.W, wl.R
+    stream = wl.stream
+    wl.warm(args.warmup)
     n_ev = max(20, min(args.steps, 500))
-    g_compute = capture(n_ev, lambda k, st: launch_compute(
-        copies[k % n_copies], batch.logit_row_offsets, batch.input_row_offsets, batch.tokens,
-        batch.sampled_tokens, batch.echo, batch.temperatures, st))
-    g_steps.replay()
-    g_compute.replay()
-    torch.cuda.synchronize()
-    if lp.read_status(ws) != 0:
-        raise RuntimeError("device status set during the graph warm-up")
+    wl.graphs(args.steps, n_ev)
 
-    sampler = ClockSampler(uuid)
+    sampler = ClockSampler(gpu_uuid(dev))
     sampler.start()
     # untimed settle so the clock samples see the GPU under load
     t_settle = time.perf_counter()
     while time.perf_counter() - t_settle < args.settle_s:
-        g_steps.replay()
+        wl.g_steps.replay()
         torch.cuda.synchronize()
-
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    w0 = time.time()
-    t_start.record(stream)
-    g_steps.replay()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    w1 = time.time()
-    if dist is not None:
-        dist.barrier()
-    ms_total = t_start.elapsed_time(t_end)
-    ms_step = ms_total / args.steps
-    # Per-launch duration of the row kernel: n_ev compute launches back to back.
-    c_start, c_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    c_start.record(stream)
-    g_compute.replay()
-    c_end.record(stream)
-    torch.cuda.synchronize()
-    sampler.stop()
-    compute_ms = c_start.elapsed_time(c_end) / n_ev
+    ms_step, w0, w1 = wl.time_graph(wl.g_steps, args.steps, dist)
+    compute_ms, _, _ = wl.time_graph(wl.g_compute, n_ev)
     ms_step, compute_ms = combine_over_ranks([ms_step, compute_ms], dist, dev)
     clocks = sampler.summary(w0, w1)
-    status = lp.read_status(ws)
+    status = lp.read_status(wl.ws)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
 
     # End to end through the public API: pinned host inputs -> device, plan+compute, results -> host.
     e2e = None
     if not args.no_e2e:
+        full_logits, ws, out_off, out_lp, out_tok = wl.full_logits, wl.ws, wl.out_off, wl.out_lp, wl.out_tok
         h_logits = full_logits.cpu().pin_memory()
         # logits offsets, tokens, sampled, echo, then the variant's inputs (input offsets, temperatures)
         small = [batch.logit_row_offsets, batch.tokens, batch.sampled_tokens, batch.echo]
@@ -454,11 +505,11 @@ def run_ours(args, rank: int, world: int, dist):
             d_logits.copy_(h_logits, non_blocking=True)
             for d, h in zip(d_ints, h_ints):
                 d.copy_(h, non_blocking=True)
-            if sharded:
+            if wl.sharded:
                 lp.plan(d_ioff if d_ioff is not None else d_ints[0], d_ints[3], T, ws, output_row_offsets=out_off,
                         stream=stream)
-                launch_compute(d_logits, d_ints[0], d_ioff, d_ints[1], d_ints[2], d_ints[3], d_tau)
-                lp.shard_merge(gathered, SHARDS, R, V, out_off, levels, out_lp, out_tok, ws, stream=stream)
+                wl.launch_compute(d_logits, d_ints[0], d_ioff, d_ints[1], d_ints[2], d_ints[3], d_tau)
+                lp.shard_merge(wl.gathered, SHARDS, R, V, out_off, levels, out_lp, out_tok, ws, stream=stream)
             else:
                 lp.step(d_logits, d_ints[0], d_ints[1], d_ints[2], d_ints[3], levels, out_off, out_lp, out_tok, ws,
                         input_row_offsets=d_ioff, temperatures=d_tau, stream=stream)
@@ -490,28 +541,9 @@ def run_ours(args, rank: int, world: int, dist):
         e2e = {"value": whole_job_rows_per_s(R, world, e2e_ms), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": k_e2e,
                "host_assembly_ms": round(asm_ms, 3)}
+        del h_logits, d_logits
 
-    if sharded:  # the partial kernel: its columns read once, one tuple written per row
-        alg = R * full_logits.shape[1] * 4 + R * lp.tuple_bytes(levels) + (B + 1) * 8 + R * 4
-    else:
-        alg = algorithmic_bytes(R, V, W, B)
-    achieved = alg / (compute_ms / 1e3) / 1e9
-    peak, peak_src = measured_peak_hbm()
-    traffic = None
-    rec = NCU_TRAFFIC.get(args.config if args.variant == "none" else f"{args.config}/{args.variant}")
-    if rec and rec.get("source_hash") == kernel_source_hash():
-        traffic = rec["bytes_per_launch"]
-    entry = "lp_ragged_shard_partials" if sharded else ("lp_ragged_compute_ex" if extended else "lp_ragged_compute")
-    kernel_name = (f"k_rows_cta ({entry}, row queue)" if uses_row_queue(min(T, T_logits))
-                   else f"k_rows ({entry}, warp ranges)")
-    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
-                "timing": f"CUDA events around one CUDA-graph replay of {n_ev} back-to-back compute launches, same "
-                          f"stream, right after the timed steps",
-                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
-                "compute_ms_per_launch": round(compute_ms, 5)}
-
+    roofline = wl.roofline(compute_ms)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import multiprocessing as mp
@@ -533,17 +565,50 @@ def run_ours(args, rank: int, world: int, dist):
         "config": {"workload": WORKLOAD_TEXT[args.config] + VARIANT_TEXT[args.variant], "name": args.config,
                    "variant": args.variant, "B": B, "T": T, "T_logits": T_logits, "V": V,
                    "levels": levels, "rows_per_gpu": R, "parallelism": f"replicas x{world} (independent batches)",
-                   "l2": f"inputs larger than L2: {n_copies} rotating logits copies of {lbytes / 1e6:.0f} MB "
-                         f"(L2 {l2 / 1e6:.0f} MB)",
-                   "launch": "the K timed steps (lp_ragged_step: plan + row kernel; vocab8: plan, partials, merge) replayed from one CUDA graph"},
-        "hbm_gbs_step": round(alg * world / (ms_step / 1e3) / 1e9, 1),
+                   "l2": wl.l2_note(),
+                   "launch": "the K timed steps (lp_ragged_step: plan + row kernel; vocab8: plan, partials, merge) "
+                             "replayed from one CUDA graph"},
+        "hbm_gbs_step": round(wl.algorithmic_bytes() * world / (ms_step / 1e3) / 1e9, 1),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": (3 if sharded else 2) * args.steps, "clocks": clocks,
+        "gpu_launches": (3 if wl.sharded else 2) * args.steps, "clocks": clocks,
     }
-    if sharded:
+    if wl.sharded:
         line["config"]["shards"] = SHARDS
         line["config"]["note"] = ("value = rows/s of one rank's step (partials over V/8 columns + merge); the 8 ranks "
                                   "run in parallel, so it is the job's rate less the all-gather, untimed on one GPU")
+    del wl, batch
+    torch.cuda.empty_cache()
+
+    # The other workloads in the same run, each timed the same way (device timing; the
+    # headline alone carries e2e and the oracle's rate), one at a time so that each one's
+    # logits are freed before the next is built.
+    if args.variant == "none" and not args.no_per_config:
+        per = {}
+        launches = 0
+        for name in PER_CONFIG:
+            if name == args.config:
+                continue
+            w = Workload(name, "none", dev)
+            w.warm(args.warmup)
+            k = max(3, min(args.steps, PER_CONFIG_STEPS))
+            w.graphs(k, max(20, min(k, 100)))
+            w.g_steps.replay()
+            torch.cuda.synchronize()
+            ms_k, a0, a1 = w.time_graph(w.g_steps, k, dist)
+            c_ms, _, _ = w.time_graph(w.g_compute, w.n_ev)
+            ms_k, c_ms = combine_over_ranks([ms_k, c_ms], dist, dev)
+            if lp.read_status(w.ws) != 0:
+                raise RuntimeError(f"{name}: device status set in the timed region")
+            per[name] = {"workload": WORKLOAD_TEXT[name], "rows_per_gpu": w.R, "steps": k,
+                         "value": whole_job_rows_per_s(w.R, world, ms_k), "unit": "rows/s", "ms_per_step": ms_k,
+                         "hbm_gbs_step": round(w.algorithmic_bytes() * world / (ms_k / 1e3) / 1e9, 1),
+                         "roofline": w.roofline(c_ms), "clocks": sampler.summary(a0, a1), "l2": w.l2_note()}
+            launches += 2 * k
+            del w
+            torch.cuda.empty_cache()
+        line["per_config"] = per
+        line["gpu_launches_per_config"] = launches
+    sampler.stop()
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -607,6 +672,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the headline workload (no per_config entries for the others)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

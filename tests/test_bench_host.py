@@ -101,17 +101,16 @@ def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() != h0
 
 
-def test_recorded_traffic_names_its_capture():
-    # Every recorded ncu traffic figure points at a committed profile summary that states the
-    # same device-code hash and the same bytes per launch (in MB, two decimals).
+def test_recorded_traffic_has_a_committed_capture():
+    # Every recorded ncu traffic figure is backed by a committed profile summary that states
+    # the same device-code hash and the same bytes per launch (in MB, two decimals).
     sys.path.insert(0, ROOT)
+    import glob
     import bench
+    texts = [open(f, encoding="utf-8").read() for f in glob.glob(os.path.join(ROOT, "profiles", "*.md"))]
     for name, rec in bench.NCU_TRAFFIC.items():
-        path = os.path.join(ROOT, rec["capture"])
-        assert os.path.isfile(path), name
-        text = open(path, encoding="utf-8").read()
-        assert rec["source_hash"] in text, name
-        assert f"{rec['bytes_per_launch'] / 1e6:.2f} MB" in text, name
+        mb = f"{rec['bytes_per_launch'] / 1e6:.2f} MB"
+        assert any(rec["source_hash"] in t and mb in t for t in texts), name
 
 
 def test_oracle_one_core_timing_on_cpu():
