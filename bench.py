@@ -423,12 +423,11 @@ class Workload:
         entry = ("lp_ragged_shard_partials" if self.sharded else
                  ("lp_ragged_compute_ex" if self.extended else "lp_ragged_compute"))
         forced = os.environ.get("LP_RAGGED_KERNEL")
-        if forced in ("warp", "queue", "span"):
+        if forced in ("warp", "queue"):
             kind = forced
         else:
             kind = "queue" if few_rows(min(self.T, self.T_logits)) else "warp"
-        kernel_name = {"warp": f"k_rows ({entry}, warp ranges)", "queue": f"k_rows_cta ({entry}, row queue)",
-                       "span": f"k_rows_span ({entry}, balanced spans)"}[kind]
+        kernel_name = {"warp": f"k_rows ({entry}, warp ranges)", "queue": f"k_rows_cta ({entry}, row queue)"}[kind]
         return {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                 "timing": f"CUDA events around one CUDA-graph replay of {self.n_ev} back-to-back compute launches, "
                           f"same stream, right after the timed steps",

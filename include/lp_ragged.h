@@ -56,9 +56,7 @@ typedef enum lp_status {
     LP_ERR_TOKEN_RANGE = 5,  /* device: an actual or sampled token >= V                     */
     LP_ERR_WORKSPACE = 6,    /* workspace NULL or smaller than lp_ragged_workspace_size     */
     LP_ERR_CUDA = 7,         /* a CUDA launch or copy failed                                */
-    LP_ERR_TEMPERATURE = 8,  /* device: a temperature that is not a positive finite number  */
-    LP_ERR_TIMEOUT = 9       /* device: a wait for a bulk copy into shared memory gave up
-                                (0.5 s; never expected): the launch wrote no further rows   */
+    LP_ERR_TEMPERATURE = 8   /* device: a temperature that is not a positive finite number  */
 } lp_status;
 
 #define LP_MAX_LEVELS 6u

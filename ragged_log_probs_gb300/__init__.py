@@ -30,7 +30,7 @@ LP_MAX_LEVELS = 6
 PAD_TOKEN = 0xFFFFFFFF
 STATUS_NAMES = {
     0: "LP_OK", 1: "LP_ERR_NULL", 2: "LP_ERR_LEVELS", 3: "LP_ERR_SHAPE", 4: "LP_ERR_OFFSETS",
-    5: "LP_ERR_TOKEN_RANGE", 6: "LP_ERR_WORKSPACE", 7: "LP_ERR_CUDA", 8: "LP_ERR_TEMPERATURE", 9: "LP_ERR_TIMEOUT",
+    5: "LP_ERR_TOKEN_RANGE", 6: "LP_ERR_WORKSPACE", 7: "LP_ERR_CUDA", 8: "LP_ERR_TEMPERATURE",
 }
 EXPORTS = ("lp_ragged_workspace_size", "lp_ragged_plan", "lp_ragged_compute", "lp_ragged_compute_ex",
            "lp_ragged_step", "lp_ragged_tuple_bytes", "lp_ragged_shard_partials", "lp_ragged_shard_merge",

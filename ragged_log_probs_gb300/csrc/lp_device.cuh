@@ -69,6 +69,11 @@ template <int U>
 __device__ __forceinline__ void cp_async16_run_pad(uint32_t dst, const float* src, int n) {
     cp_async16_seq_pad(dst, src, n, std::make_integer_sequence<int, U>{});
 }
+// Asynchronous 4-byte global -> shared copy (an index or a status word fetched while
+// the thread goes on; visible to it after its cp.async.wait_group).
+__device__ __forceinline__ void cp_async4(uint32_t smem_addr, const void* gptr) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr), "l"(gptr) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -85,65 +90,6 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // wait for (gptr 16-byte aligned, bytes a multiple of 16, the range inside one allocation).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* gptr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
-}
-
-// ---- bulk copies into a shared-memory ring (one producer thread, mbarrier handshakes) ----
-// Every wait on an mbarrier is bounded in time (%globaltimer): a wait that gives up
-// returns false and the caller takes its abort path; no wait can spin forever.
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-// Makes the initialised barriers visible to the bulk-copy (async) proxy.
-__device__ __forceinline__ void mbar_init_fence() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Wait for the phase of parity `parity` of barrier `bar` to complete, for at most
-// limit_ns after the first failed try; *abort (shared) ends the wait early.
-// Returns false when it gave up or was aborted.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const volatile uint32_t* abort,
-                                                  uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u) {
-            if (*abort) return false;
-            if (global_ns() - t0 > limit_ns) return false;
-        }
-    }
-}
-// One bulk copy global -> shared of `bytes` (16-byte aligned addresses, a multiple of
-// 16 bytes) that completes `bytes` of transaction count on barrier `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-// Barrier `id` (1..15) among `nthreads` threads, whole warps, that execute it.
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ bool better(float xa, uint32_t ia, float xb, uint32_t ib) {

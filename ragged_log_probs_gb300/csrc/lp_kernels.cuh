@@ -53,6 +53,20 @@ namespace lpk {
 #ifndef LP_QUEUE_UNROLL
 #define LP_QUEUE_UNROLL 4  // vectors per lane per block in the row-queue kernel
 #endif
+#ifndef LP_NEXT_TOKEN_FAST
+#define LP_NEXT_TOKEN_FAST 1  // row queue: next-token compute launches stream before reading offsets
+#endif
+#ifndef LP_EARLY_TRIGGER
+#define LP_EARLY_TRIGGER 1  // row kernels let their programmatic dependents launch at once
+#endif
+
+// A row kernel lets the next kernel on the stream, when that one is launched as a
+// programmatic dependent, become resident on SMs this launch no longer uses (its tail);
+// such a dependent waits in griddepcontrol.wait for this launch to finish and flush
+// before it reads anything, so this only hides its launch.
+__device__ __forceinline__ void trigger_dependents() {
+    if (LP_EARLY_TRIGGER) pdl_launch_dependents();
+}
 
 
 constexpr int kWarps = 8;
@@ -65,7 +79,6 @@ constexpr int kPlanThreads = 1024;
 constexpr uint32_t kStatusOffsets = 1u << 4;     // bit of LP_ERR_OFFSETS
 constexpr uint32_t kStatusTokenRange = 1u << 5;  // bit of LP_ERR_TOKEN_RANGE
 constexpr uint32_t kStatusTemperature = 1u << 8; // bit of LP_ERR_TEMPERATURE
-constexpr uint32_t kStatusTimeout = 1u << 9;     // bit of LP_ERR_TIMEOUT
 
 // Workspace: [header 256 B][arrival counters u32 x max warps, zeroed by plan, padded
 // to 256 B][partial slots].
@@ -118,13 +131,10 @@ struct RowsParams {
     // counters or the status word.
     uint32_t early;
     uint32_t out_rows;       // rows out_lp / out_tok hold (0: not checked)
-    // Balanced-span kernel (k_rows_span):
-    uint32_t stages;         // ring stages of kSpanChunkBytes
-    uint32_t next_token;     // 1: one logits row per batch and per position (T == T_logits == B, no
-                             // separate positions): valid offsets are then 0..B and output row o
-                             // reads logits row o, so the copies start before any offset is read
-    uint32_t drop_chunk;     // test of the bounded waits: the copy of this chunk of each CTA is never
-                             // issued (0xFFFFFFFF: none), so its wait runs out and LP_ERR_TIMEOUT is set
+    // Row-queue kernel, compute launch on next-token logits (T == T_logits == B, every
+    // position its own logits row): valid offsets are then 0..B, so output row o is batch
+    // o and reads logits row o, and a CTA streams its first task before any offset is read.
+    uint32_t next_token;
 };
 
 // Row tuple of one vocab shard (lp_ragged_shard_partials), u32 words:
@@ -1010,6 +1020,7 @@ __host__ __device__ constexpr uint32_t ring_bytes() { return (uint32_t)kWarps * 
 template <int SLOTS, bool TOPK, int U, int STAGES, bool EXT>
 __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) {
     extern __shared__ __align__(128) unsigned char s_raw[];
+    trigger_dependents();
     float4* rings = reinterpret_cast<float4*>(s_raw);
     uint32_t* s_dyn = reinterpret_cast<uint32_t*>(s_raw + ring_bytes<U, STAGES>());
     __shared__ float s_cx[kWarps][64];
@@ -1140,7 +1151,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
 // for the top-k threshold (see stream_piece). The last CTA to leave resets the queue
 // words for the next call; the merging CTA resets its row's ticket.
 template <int NW>
-struct CtaMerge {
+struct __align__(128) CtaMerge {
     float list_x[NW][64];
     uint32_t list_i[NW][64];
     float red_c[NW];
@@ -1150,6 +1161,9 @@ struct CtaMerge {
     uint32_t row;
     uint32_t thr;  // threshold shared by the warps of the CTA for the current row
     uint32_t last;  // this CTA took the last ticket of its split row
+    uint32_t status, rows;  // the status word and R, read once for the whole CTA
+    uint32_t fast_ok;  // next-token start: 2 unchecked, 1 the layout is valid, 0 it is not
+    uint32_t chk[2];   // next-token start: output_row_offsets[o], [o + 1] of the current task
     float lane_max[NW][32];  // running lane maxima of the current row (-inf between rows)
 };
 
@@ -1185,6 +1199,7 @@ constexpr int kQueueUnroll = LP_QUEUE_UNROLL;
 template <int SLOTS, bool TOPK, int U, int STAGES, int NW, bool EXT>
 __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     extern __shared__ __align__(128) unsigned char s_raw[];
+    trigger_dependents();
     float4* rings = reinterpret_cast<float4*>(s_raw);
     uint32_t* s_dyn = reinterpret_cast<uint32_t*>(s_raw + (size_t)NW * STAGES * U * 512u);
     __shared__ float s_cx[NW][64];
@@ -1199,6 +1214,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const uint32_t* out_off = p.out_off;
     const uint8_t* echo = p.echo;
     const bool early = p.early && p.stage_offsets;
+    const bool fast = LP_NEXT_TOKEN_FAST && p.next_token != 0u && !p.early;
     uint32_t status, R;
     if (early) {
         // The logits are complete (the plan, launched after all earlier work, is running).
@@ -1207,11 +1223,30 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         bool bad;
         stage_and_scan<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo, R, bad);
         status = bad ? kStatusOffsets : 0u;
+    } else if (fast) {
+        pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
+        // Next-token logits: the tasks are known without the offsets (see
+        // RowsParams::next_token). The plan's status and the caller's row count arrive in
+        // shared memory while the first task streams and are checked before any row is
+        // written (a rejected layout writes nothing, as below).
+        status = 0u;
+        R = B;
+        if (threadIdx.x == 0) {
+            cp_async4((uint32_t)__cvta_generic_to_shared(&cm.status), p.status);
+            cp_async4((uint32_t)__cvta_generic_to_shared(&cm.rows), out_off + B);
+        }
     } else {
         pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
-        status = __ldcg(p.status);
-        R = __ldcg(p.out_off + B);
+        // one read for the whole CTA: other CTAs may set status bits meanwhile, and every
+        // thread must leave the task loop below on the same task count
+        if (threadIdx.x == 0) {
+            cm.status = __ldcg(p.status);
+            cm.rows = __ldcg(p.out_off + B);
+        }
         if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo);
+        __syncthreads();
+        status = cm.status;
+        R = cm.rows;
     }
     cm.lane_max[w][lane] = neg_inf();
     // Tasks: piece `task % S` of row `task / S` (S = p.split pieces per row). The launch
@@ -1237,6 +1272,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     if (threadIdx.x == 0) {
         cm.has_xt = 0u;
         cm.thr = 0u;
+        cm.fast_ok = 2u;
         uint32_t task = ntask;
         if (blockIdx.x < nA) task = blockIdx.x;
         else if (ntask > nA) task = next_task();
@@ -1283,8 +1319,26 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         const uint32_t task = cm.row;
         if (task >= ntask) break;
         const uint32_t o = S == 1u ? task : task / S, piece = task - o * S;
-        const uint32_t lo = batch_of_row(out_off, B, o, p.stage_offsets != 0u, lane);
-        const RowDesc d = describe_row<EXT>(p, off, loff, out_off, echo, lo, o);
+        RowDesc d;
+        if (fast) {
+            d.rowp = p.logits + (size_t)o * V;
+            d.t = p.sampled[o];
+            d.k = kLog2e;
+            d.tau = 1.f;
+            d.err = 0u;  // the row's checks come before its write
+            if (EXT && p.tau != nullptr) {
+                d.tau = p.tau[o];
+                d.k = __fdiv_rn(kLog2e, d.tau);
+            }
+            if (threadIdx.x == 0) {  // the caller's output offsets of row o, fetched meanwhile
+                cp_async4((uint32_t)__cvta_generic_to_shared(&cm.chk[0]), out_off + o);
+                cp_async4((uint32_t)__cvta_generic_to_shared(&cm.chk[1]), out_off + o + 1);
+                cp_async_commit();
+            }
+        } else {
+            const uint32_t lo = batch_of_row(out_off, B, o, p.stage_offsets != 0u, lane);
+            d = describe_row<EXT>(p, off, loff, out_off, echo, lo, o);
+        }
         if (d.err) {
             if (early) pdl_wait();  // before any status write or queue access
             if (w == 0 && piece == 0) emit_invalid<EXT>(p, o, d.err, lane);
@@ -1328,7 +1382,34 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             for (int j = lane; j < NW; j += 32) lse2_combine(C, Sm, cm.red_c[j], cm.red_s[j]);
             warp_lse2_reduce(C, Sm);
             uint32_t last = 0u;
-            if (S == 1) {
+            bool write = true;       // fast start: the layout is valid
+            uint32_t row_err = 0u;   // fast start: this row's own check
+            if (fast) {
+                uint32_t ok = 0u, c0 = 0u, c1 = 0u;
+                if (lane == 0) {
+                    cp_async_wait<0>();
+                    if (cm.fast_ok == 2u) {  // first task: the plan's check and the caller's row count
+                        const bool st_ok = (cm.status & kStatusOffsets) == 0u;
+                        cm.fast_ok = (st_ok && cm.rows == B) ? 1u : 0u;
+                        if (st_ok && cm.rows != B) atomicOr(p.status, kStatusOffsets);
+                    }
+                    ok = cm.fast_ok;
+                    c0 = cm.chk[0];
+                    c1 = cm.chk[1];
+                }
+                write = __shfl_sync(kFull, ok, 0) == 1u;
+                c0 = __shfl_sync(kFull, c0, 0);
+                c1 = __shfl_sync(kFull, c1, 0);
+                if (!(c0 == o && c1 == o + 1u)) row_err = kStatusOffsets;
+                else if (EXT && p.tau != nullptr &&
+                         !(d.tau > 0.f && d.tau <= 3.4028234663852886e38f && d.k <= 3.4028234663852886e38f))
+                    row_err = kStatusTemperature;
+            }
+            if (!write) {
+                // a layout the plan rejects: nothing written, nothing published
+            } else if (row_err) {
+                if (piece == 0) emit_invalid<EXT>(p, o, row_err, lane);
+            } else if (S == 1) {
                 if (EXT && p.tuple_out != nullptr)
                     store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, lane);
                 else
@@ -1406,495 +1487,6 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             queue[0] = 0u;
             queue[1] = 0u;
         }
-    }
-}
-
-// ---------------------------------------------------------------------------------
-// Few rows (decode batches), balanced over the SMs: one CTA per SM. The scored rows
-// form the vector space [0, R*nq) in row-major order and CTA c owns the contiguous span
-// [c*Q/G, (c+1)*Q/G), so every SM streams the same number of bytes (with whole rows per
-// CTA, 256 decode rows on 152 SMs left 104 SMs with two rows and 48 with one). A row
-// is cut only at span ends; the CTAs holding its pieces publish them and the CTA that
-// takes the row's last ticket merges them, as in k_rows. No CTA waits on another.
-//
-// A CTA runs three roles over the same walk of its span (rows, then 32 KB chunks):
-//  * a producer thread moves the span through a ring of `stages` stages with bulk
-//    copies (cp.async.bulk; each copy completes its bytes on its stage's "full"
-//    mbarrier) and reuses a stage once its "empty" mbarrier says every consumer is done;
-//  * kSpanWarps consumer warps each reduce 2 KB (4 vectors per lane) of every stage; at
-//    the end of a row piece they merge their results in shared memory (a tree over
-//    named barriers) and hand the piece's (reference, sum, top-k list) to
-//  * a finisher warp, which adds the row's partial edge vectors and the target logit,
-//    checks the layout, and writes the row or publishes the piece (ticket, merge).
-// The consumers never touch global memory besides the ring and never wait on the
-// finisher except for the parity slot they are about to refill, so the copies keep
-// ~190 KB in flight per SM whatever the row ends cost. Every mbarrier wait is bounded in
-// time: a wait that gives up sets LP_ERR_TIMEOUT and the CTA's abort word; the producer
-// then stops issuing and waits (bounded again) for its copies in flight, and the other
-// warps run on through the same barrier schedule without waiting and write nothing.
-#ifndef LP_SPAN_WARPS
-#define LP_SPAN_WARPS 16  // consumer warps of the balanced-span kernel
-#endif
-#ifndef LP_SPAN_U
-#define LP_SPAN_U 4  // 16-byte vectors per consumer lane and stage
-#endif
-#ifndef LP_SPAN_COPIES
-#define LP_SPAN_COPIES 1  // bulk copies a stage is filled with
-#endif
-constexpr int kSpanWarps = LP_SPAN_WARPS;
-constexpr int kSpanU = LP_SPAN_U;
-constexpr uint32_t kSpanCopies = LP_SPAN_COPIES;
-constexpr int kSpanProducer = kSpanWarps;                       // warp index of the producer
-constexpr int kSpanFinisher = kSpanWarps + 1;                   // warp index of the finisher
-constexpr int kSpanThreads = (kSpanWarps + 2) * 32;
-constexpr uint32_t kSpanVecPerWarp = 32u * kSpanU;              // 16-byte vectors per warp and stage
-constexpr uint32_t kSpanChunkVec = kSpanWarps * kSpanVecPerWarp;
-constexpr uint32_t kSpanChunkBytes = kSpanChunkVec * 16u;       // bytes per stage (32 KB by default)
-constexpr uint32_t kSpanMaxStages = 16;
-constexpr uint64_t kSpanWaitNs = 500ull * 1000ull * 1000ull;    // 0.5 s: only a broken pipeline waits this long
-
-struct __align__(128) SpanShared {
-    uint64_t full[kSpanMaxStages];   // stage s holds its copy (producer's expect_tx + the copy's bytes)
-    uint64_t empty[kSpanMaxStages];  // stage s has been read by every consumer warp
-    uint64_t row_done[2];            // by row parity: the consumers' result of a row piece is ready
-    uint64_t slot_free[2];           // by row parity: the finisher has taken that result
-    float red_c[2][kSpanWarps];      // per-warp (reference, sum) of a row piece, by row parity
-    float red_s[2][kSpanWarps];
-    uint32_t thr[2];                 // top-k threshold shared by the consumer warps (f2ord; 0: none)
-    uint32_t abort;                  // a wait gave up: no more copies, no more writes
-    uint32_t status, rows;           // the status word and R as thread 0 read them (one value per CTA)
-    uint32_t pad[11];
-    float list_x[2][kSpanWarps][64];  // warps' sorted lists, merged by a tree into [p][0]
-    uint32_t list_i[2][kSpanWarps][64];
-    float lane_max[2][kSpanWarps][32];  // running lane maxima of the row (-inf between rows)
-    float cx[kSpanWarps][64];        // per-warp candidate buffers of the top-k selection
-    uint32_t ci[kSpanWarps][64];
-};
-
-// Bounds of output row o's piece in the span [g0, g1) (row-relative vectors [q0, q1)),
-// and the piece's whole 16-byte vectors [qa, qb) for a row starting `a` floats past a
-// 16-byte boundary (the row's partial first and last vectors lie outside [qa, qb)).
-struct SpanPiece {
-    uint32_t q0, q1, qa, qb;
-    int a;
-};
-__device__ __forceinline__ SpanPiece span_piece(uint64_t g0, uint64_t g1, uint32_t o, uint32_t nq, uint32_t V,
-                                                const float* rowp) {
-    SpanPiece pc;
-    const uint64_t rs = (uint64_t)o * nq;
-    pc.q0 = (uint32_t)((g0 > rs ? g0 : rs) - rs);
-    pc.q1 = (uint32_t)((g1 < rs + nq ? g1 : rs + nq) - rs);
-    pc.a = (int)(((uintptr_t)rowp >> 2) & 3u);
-    const uint32_t qf = pc.a ? 1u : 0u, qe = (V + (uint32_t)pc.a) >> 2;
-    pc.qa = max(pc.q0, qf);
-    pc.qb = max(min(pc.q1, qe), pc.qa);
-    return pc;
-}
-
-// Row descriptor of the span walk, the same in every role. Next-token logits: output
-// row o is batch o and logits row o (the layout is checked by the finisher before any
-// row is written); otherwise describe_row on the (staged) batch arrays.
-template <bool EXT>
-__device__ __forceinline__ RowDesc span_row(const RowsParams& p, bool fast, const uint32_t* off, const uint32_t* loff,
-                                            const uint32_t* out_off, const uint8_t* echo, uint32_t o, int lane,
-                                            bool want_target) {
-    RowDesc d;
-    if (fast) {
-        d.rowp = p.logits + (size_t)o * p.V;
-        d.t = want_target ? p.sampled[o] : 0u;
-        d.k = kLog2e;
-        d.tau = 1.f;
-        d.err = 0u;
-        if (EXT && p.tau != nullptr) {
-            const float tau = p.tau[o];
-            d.tau = tau;
-            d.k = __fdiv_rn(kLog2e, tau);
-        }
-        return d;
-    }
-    const uint32_t b = batch_of_row(out_off, p.B, o, p.stage_offsets != 0u, lane);
-    return describe_row<EXT>(p, off, loff, out_off, echo, b, o);
-}
-
-template <int SLOTS, bool TOPK, bool EXT>
-__global__ void __launch_bounds__(kSpanThreads, 1) k_rows_span(RowsParams p) {
-    extern __shared__ __align__(128) unsigned char s_raw[];
-    __shared__ SpanShared sh;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t B = p.B, V = p.V, K = p.K, NS = p.stages;
-    const bool fast = p.next_token != 0u;
-    const bool early = p.early && (fast || p.stage_offsets);
-    uint32_t* s_dyn = reinterpret_cast<uint32_t*>(s_raw + (size_t)NS * kSpanChunkBytes);
-    const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(s_raw);
-    const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(&sh.full[0]);
-    const uint32_t empty0 = (uint32_t)__cvta_generic_to_shared(&sh.empty[0]);
-    const uint32_t done0 = (uint32_t)__cvta_generic_to_shared(&sh.row_done[0]);
-    const uint32_t free0 = (uint32_t)__cvta_generic_to_shared(&sh.slot_free[0]);
-    volatile uint32_t* abort_w = &sh.abort;
-
-    if (threadIdx.x == 0) {
-        for (uint32_t s = 0; s < NS; ++s) {
-            mbar_init(full0 + 8u * s, 1u);
-            mbar_init(empty0 + 8u * s, (uint32_t)kSpanWarps);
-        }
-        for (uint32_t q = 0; q < 2; ++q) {
-            mbar_init(done0 + 8u * q, 1u);
-            mbar_init(free0 + 8u * q, 1u);
-            sh.thr[q] = 0u;
-        }
-        sh.abort = 0u;
-        mbar_init_fence();
-    }
-    if (w < kSpanWarps) {
-        sh.lane_max[0][w][lane] = neg_inf();
-        sh.lane_max[1][w][lane] = neg_inf();
-    }
-
-    // ---- the rows: R and the layout ----------------------------------------------------
-    const uint32_t* off = p.off;
-    const uint32_t* loff = p.loff;
-    const uint32_t* out_off = p.out_off;
-    const uint8_t* echo = p.echo;
-    uint32_t R, status = 0u;
-    if (fast) {
-        // Valid offsets (the plan's check, read before any row is written) are 0..B here:
-        // B ranges, each non-empty, inside T == B positions.
-        if (!early) pdl_wait();
-        R = B;
-    } else if (early) {
-        bool bad;
-        stage_and_scan<EXT>(p, s_dyn, threadIdx.x, kSpanThreads, off, loff, out_off, echo, R, bad);
-        status = bad ? kStatusOffsets : 0u;
-    } else {
-        pdl_wait();
-        // one read for the whole CTA: other CTAs may set status bits meanwhile, and every
-        // thread must take the same early exit below
-        if (threadIdx.x == 0) {
-            sh.status = __ldcg(p.status);
-            sh.rows = __ldcg(p.out_off + B);
-        }
-        if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kSpanThreads, off, loff, out_off, echo);
-    }
-    __syncthreads();  // barriers initialised, batch arrays staged
-    if (!fast && !early) {
-        status = sh.status;
-        R = sh.rows;
-    }
-    if (status & kStatusOffsets) return;  // the plan rejects the offsets
-    if (R == 0) return;
-    if (R > p.T || (EXT && p.tuple_out != nullptr && R > p.tuple_rows) || (p.out_rows && R > p.out_rows)) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) {
-            pdl_wait();
-            atomicOr(p.status, kStatusOffsets);
-        }
-        return;
-    }
-    const uint32_t nq = p.nq;
-    const uint64_t Q = (uint64_t)R * nq;
-    uint64_t G = (Q + p.min_piece - 1) / p.min_piece;  // spans of min_piece vectors at least
-    if (G > gridDim.x) G = gridDim.x;
-    if (G == 0) G = 1;
-    if (blockIdx.x >= G) return;
-    const uint64_t g0 = sk_start(blockIdx.x, Q, G), g1 = sk_start(blockIdx.x + 1, Q, G);
-    if (g0 >= g1) return;
-    const uint32_t o_first = (uint32_t)(g0 / nq), o_last = (uint32_t)((g1 - 1) / nq);
-    // No CTA-wide barrier after this point: the three roles run the same walk over the
-    // span's rows and chunks, so they agree on every chunk and every row piece.
-
-    if (w == kSpanProducer) {
-        // ---- producer warp: lane 0 issues the copies ----------------------------------
-        uint32_t i = 0, s = 0, rnd = 0;  // chunks issued; stage and round of the next one
-        bool ok = true;
-        for (uint32_t o = o_first; o <= o_last && ok; ++o) {
-            const RowDesc d = span_row<EXT>(p, fast, off, loff, out_off, echo, o, lane, false);
-            if (d.err) continue;  // no copies: the finisher emits the invalid row
-            const SpanPiece pc = span_piece(g0, g1, o, nq, V, d.rowp);
-            const float* vbase = d.rowp - pc.a;
-            for (uint32_t qc = pc.qa; qc < pc.qb && ok; qc += kSpanChunkVec) {
-                const uint32_t n = min(kSpanChunkVec, pc.qb - qc);
-                if (lane == 0) {
-                    if (rnd > 0 && !mbar_wait_bounded(empty0 + 8u * s, (rnd - 1u) & 1u, abort_w, kSpanWaitNs)) {
-                        ok = false;
-                    } else if (*abort_w) {
-                        ok = false;
-                    } else if (i != p.drop_chunk) {
-                        mbar_arrive_expect_tx(full0 + 8u * s, n * 16u);
-                        if constexpr (kSpanCopies == 1) {
-                            bulk_copy_g2s(ring_s + s * kSpanChunkBytes, vbase + 4 * (size_t)qc, n * 16u,
-                                          full0 + 8u * s);
-                        } else {
-                            const uint32_t per = (n + kSpanCopies - 1) / kSpanCopies;
-                            for (uint32_t c0 = 0; c0 < n; c0 += per) {
-                                const uint32_t m = min(per, n - c0);
-                                bulk_copy_g2s(ring_s + s * kSpanChunkBytes + 16u * c0, vbase + 4 * (size_t)(qc + c0),
-                                              m * 16u, full0 + 8u * s);
-                            }
-                        }
-                    }
-                }
-                ok = __shfl_sync(kFull, ok, 0);
-                if (ok) {
-                    ++i;
-                    if (++s == NS) { s = 0; ++rnd; }
-                }
-            }
-        }
-        if (!ok && lane == 0) {
-            // A wait gave up: record it, tell the other warps, and wait (bounded) for the
-            // copies in flight before this thread, and so the CTA, may leave.
-            *abort_w = 1u;
-            if (early) pdl_wait();
-            atomicOr(p.status, kStatusTimeout);
-            const uint32_t zero = 0u;
-            const uint32_t last = i < NS ? i : NS;  // the last `last` chunks may be in flight
-            for (uint32_t k = 0; k < last; ++k) {
-                const uint32_t j = i - 1u - k;  // chunk j went to stage j % NS in round j / NS
-                if (j != p.drop_chunk)
-                    (void)mbar_wait_bounded(full0 + 8u * (j % NS), (j / NS) & 1u, &zero, kSpanWaitNs);
-            }
-        }
-        return;
-    }
-
-    if (w == kSpanFinisher) {
-        // ---- finisher warp: one row piece after the other ------------------------------
-        bool layout_ok = true, status_checked = !fast;
-        bool aborted = false;
-        uint32_t n_piece = 0;  // valid row pieces so far (row parity = n_piece & 1)
-        for (uint32_t o = o_first; o <= o_last; ++o) {
-            const RowDesc d = span_row<EXT>(p, fast, off, loff, out_off, echo, o, lane, true);
-            const SpanPiece pc = span_piece(g0, g1, o, nq, V, d.rowp);
-            if (early) pdl_wait();  // the plan has finished before the status, tickets or rows are touched
-            if (d.err) {  // no copies and no consumer result for this row
-                if (pc.q0 == 0 && !*abort_w) emit_invalid<EXT>(p, o, d.err, lane);
-                continue;
-            }
-            const uint32_t par = n_piece & 1u, use = n_piece >> 1;
-            ++n_piece;
-            // meanwhile: the fast path's layout checks, the target logit and the row's
-            // partial edge vectors, all global loads of this warp
-            uint32_t fast_err = 0u;
-            if (fast) {
-                if (!status_checked) {
-                    // the plan's check of the offsets, and the caller's row count (the
-                    // outputs hold output_row_offsets[B] rows: with any other count than B
-                    // no row is written)
-                    const uint32_t st = __ldcg(p.status), rc = __ldcg(p.out_off + B);
-                    layout_ok = (st & kStatusOffsets) == 0u && rc == B;
-                    if ((st & kStatusOffsets) == 0u && rc != B && lane == 0) atomicOr(p.status, kStatusOffsets);
-                    status_checked = true;
-                }
-                if (!(__ldg(out_off + o) == o && __ldg(out_off + o + 1) == o + 1u)) fast_err = kStatusOffsets;
-                else if (EXT && p.tau != nullptr &&
-                         !(d.tau > 0.f && d.tau <= 3.4028234663852886e38f && d.k <= 3.4028234663852886e38f))
-                    fast_err = kStatusTemperature;
-            }
-            const uint32_t t = d.t;
-            const uint32_t t_loc = EXT ? t - p.vocab_base : t;
-            const int64_t e_lo = 4 * (int64_t)pc.q0 - pc.a, e_hi = 4 * (int64_t)pc.q1 - pc.a;
-            const bool t_here = t_loc < V && (int64_t)t_loc >= e_lo && (int64_t)t_loc < e_hi;
-            const float xt = t_here ? __ldg(d.rowp + t_loc) : 0.f;
-            // edge vectors: at most one before [qa, qb) and one after; one element per lane
-            float ex = neg_inf();
-            uint32_t eid = kPadId;
-            {
-                // [q0, min(qa, q1)) holds at most the row's first vector and [qb, q1) at most
-                // its last two (the row's whole vectors are [qa, qb)): 12 elements at most
-                const uint32_t e_first_hi = min(pc.qa, pc.q1);
-                const uint32_t lanes_lo = 4u * (e_first_hi > pc.q0 ? e_first_hi - pc.q0 : 0u);
-                const uint32_t lanes_hi = 4u * (pc.q1 > pc.qb ? pc.q1 - pc.qb : 0u);
-                int64_t e = -1;
-                if ((uint32_t)lane < lanes_lo) e = 4 * (int64_t)pc.q0 - pc.a + lane;
-                else if ((uint32_t)lane - lanes_lo < lanes_hi) e = 4 * (int64_t)pc.qb - pc.a + (lane - lanes_lo);
-                if (e >= 0 && e < (int64_t)V) {
-                    ex = __ldg(d.rowp + e);
-                    eid = (uint32_t)e;
-                }
-            }
-            // the consumers' result of this piece
-            bool ready = aborted ? false : mbar_wait_bounded(done0 + 8u * par, use & 1u, abort_w, kSpanWaitNs);
-            ready = __all_sync(kFull, ready);
-            if (!ready && !aborted) {
-                aborted = true;
-                if (lane == 0) {
-                    *abort_w = 1u;
-                    atomicOr(p.status, kStatusTimeout);
-                }
-            }
-            float C = neg_inf(), S = 0.f;
-            for (int j = lane; j < kSpanWarps; j += 32) lse2_combine(C, S, sh.red_c[par][j], sh.red_s[par][j]);
-            WarpList<SLOTS> L;
-            L.reset();
-            if constexpr (TOPK) {
-#pragma unroll
-                for (int k = 0; k < SLOTS; ++k) {
-                    L.x[k] = sh.list_x[par][0][lane + 32 * k];
-                    L.id[k] = sh.list_i[par][0][lane + 32 * k];
-                }
-            }
-            __syncwarp();
-            if (lane == 0 && !aborted) mbar_arrive(free0 + 8u * par);  // the consumers may refill the slot
-            // the edge elements: each lane's term relative to its own reference c = fp32(x*k)
-            // (as the consumers' lane sums are formed), and one candidate per lane
-            if (ex != neg_inf()) {
-                const float ce = ex * d.k;
-                lse2_combine(C, S, ce, ex2(fmaf(ex, d.k, -ce)));
-            }
-            warp_lse2_reduce(C, S);
-            if constexpr (TOPK) {
-                if (__any_sync(kFull, eid != kPadId)) L.insert32(ex, eid, lane);
-            }
-            const float xt_row = xt;  // every lane loaded it
-            const bool write = layout_ok && !*abort_w;
-            const bool full = pc.q0 == 0 && pc.q1 == nq;
-            if (!write) continue;
-            if (fast_err) {
-                if (pc.q0 == 0) emit_invalid<EXT>(p, o, fast_err, lane);
-                continue;
-            }
-            if (full) {
-                if (EXT && p.tuple_out != nullptr)
-                    store_row_tuple<SLOTS, TOPK>(p, o, L, C, S, t, t_here, xt_row, lane);
-                else
-                    write_row<SLOTS, TOPK>(p, o, L, C, S, t, t_here, xt_row, d.k, d.tau, lane);
-                continue;
-            }
-            // a piece of a row cut by span ends: publish it; the CTA taking the row's last
-            // ticket merges all pieces
-            const uint64_t gr = (uint64_t)o * nq;
-            const uint64_t w0 = sk_owner(gr, Q, G), w1 = sk_owner(gr + nq - 1, Q, G);
-            const uint32_t pieces = (uint32_t)(w1 - w0 + 1);
-            store_piece<SLOTS, TOPK>(
-                reinterpret_cast<uint32_t*>(p.partials + (size_t)(2 * blockIdx.x + (o == o_first ? 0 : 1)) * p.stride),
-                K, L, C, S, t_here, xt_row, lane);
-            if (take_ticket(p.counters, w0, pieces, lane)) {
-                const bool tail0 = sk_start(w0, Q, G) != gr;
-                bool has_xt;
-                float xt_m;
-                merge_pieces<SLOTS, TOPK>(p, w0, pieces, tail0, lane, L, C, S, has_xt, xt_m);
-                if (lane == 0) p.counters[w0] = 0u;  // ready for the next call
-                if (EXT && p.tuple_out != nullptr)
-                    store_row_tuple<SLOTS, TOPK>(p, o, L, C, S, t, has_xt, xt_m, lane);
-                else
-                    write_row<SLOTS, TOPK>(p, o, L, C, S, t, has_xt, xt_m, d.k, d.tau, lane);
-            }
-        }
-        return;
-    }
-
-    // ---- consumer warps ---------------------------------------------------------------
-    uint32_t s = 0, rnd = 0, n_piece = 0;
-    bool aborted = false;
-    const float* ring_f = reinterpret_cast<const float*>(s_raw);
-    for (uint32_t o = o_first; o <= o_last; ++o) {
-        const RowDesc d = span_row<EXT>(p, fast, off, loff, out_off, echo, o, lane, false);
-        if (d.err) continue;  // no copies for this row; the finisher emits it
-        const SpanPiece pc = span_piece(g0, g1, o, nq, V, d.rowp);
-        const uint32_t par = n_piece & 1u, use = n_piece >> 1;
-        ++n_piece;
-
-        LaneSum ls;
-        ls.init(d.k);
-        Selector<SLOTS> sel;
-        sel.init(sh.cx[w], sh.ci[w], K);
-        uint32_t blk = 0;
-        for (uint32_t qc = pc.qa; qc < pc.qb; qc += kSpanChunkVec, ++blk) {
-            const uint32_t n = min(kSpanChunkVec, pc.qb - qc);
-            const uint32_t ws = (uint32_t)w * n / kSpanWarps, we = (uint32_t)(w + 1) * n / kSpanWarps;
-            const uint32_t len = we - ws;  // <= kSpanVecPerWarp
-            if (!aborted) {
-                const bool ready = mbar_wait_bounded(full0 + 8u * s, rnd & 1u, abort_w, kSpanWaitNs);
-                aborted = !__all_sync(kFull, ready);
-                if (aborted && lane == 0) {  // gave up (or another warp did): record it once per warp
-                    *abort_w = 1u;
-                    if (early) pdl_wait();
-                    atomicOr(p.status, kStatusTimeout);
-                }
-            }
-            // After an abort the warp reads the stages without waiting (values are discarded)
-            // and frees none of them: the producer can then never issue a copy into a stage
-            // whose previous copy may still be landing.
-            const float* stage_f = ring_f + (size_t)s * (kSpanChunkBytes / 4u) + 4u * ws;
-            const float4* stage_v = reinterpret_cast<const float4*>(stage_f);
-            float4 v[kSpanU];
-#pragma unroll
-            for (int u = 0; u < kSpanU; ++u) {
-                const uint32_t j = 32u * u + (uint32_t)lane;
-                v[u] = j < len ? stage_v[j] : make_float4(neg_inf(), neg_inf(), neg_inf(), neg_inf());
-            }
-            float mu[kSpanU];
-#pragma unroll
-            for (int u = 0; u < kSpanU; ++u) mu[u] = max4(v[u]);
-            float bm = mu[0];
-#pragma unroll
-            for (int u = 1; u + 1 < kSpanU; u += 2) bm = max3(bm, mu[u], mu[u + 1]);
-            if ((kSpanU & 1) == 0) bm = fmaxf(bm, mu[kSpanU - 1]);
-            ls.add_block<kSpanU>(v, bm);
-            const uint32_t idb = 4u * (qc + ws + (uint32_t)lane) - (uint32_t)pc.a;
-            const uint32_t id_end = 4u * (qc + we) - (uint32_t)pc.a;
-            select_block<SLOTS, TOPK, kSpanU, kSpanWarps>(v, bm, blk, len < kSpanVecPerWarp, idb, id_end, stage_f, ls,
-                                                         sel, lane, &sh.thr[par], &sh.lane_max[par][0][0], w);
-            __syncwarp();
-            if (lane == 0 && !aborted) mbar_arrive(empty0 + 8u * s);
-            if (++s == NS) { s = 0; ++rnd; }
-        }
-        if constexpr (TOPK) {
-            if (sel.cnt > 0) sel.flush(lane);
-        }
-        if (ls.m != neg_inf()) ls.rebase(ls.m);
-        float C = (ls.m == neg_inf()) ? neg_inf() : ls.ref(), S = ls.sum();
-        warp_lse2_reduce(C, S);
-        // ---- row end: this parity's slot must have been taken by the finisher (two pieces ago)
-        if (use > 0 && !aborted) {
-            const bool ready = mbar_wait_bounded(free0 + 8u * par, (use - 1u) & 1u, abort_w, kSpanWaitNs);
-            aborted = !__all_sync(kFull, ready);
-            if (aborted && lane == 0) {
-                *abort_w = 1u;
-                if (early) pdl_wait();
-                atomicOr(p.status, kStatusTimeout);
-            }
-        }
-        if (lane == 0) {
-            sh.red_c[par][w] = C;
-            sh.red_s[par][w] = S;
-        }
-        if constexpr (TOPK) {
-#pragma unroll
-            for (int k = 0; k < SLOTS; ++k) {
-                sh.list_x[par][w][lane + 32 * k] = sel.L.x[k];
-                sh.list_i[par][w][lane + 32 * k] = sel.L.id[k];
-            }
-        }
-        named_sync(1, kSpanWarps * 32);
-        // every consumer is past this row's stream: clear this parity's threshold state
-        // (its next user is the piece after next, after the next piece's barriers)
-        sh.lane_max[par][w][lane] = neg_inf();
-        if (threadIdx.x == 0) sh.thr[par] = 0u;
-        if constexpr (TOPK) {
-#pragma unroll
-            for (int st = 1; st < kSpanWarps; st <<= 1) {
-                if ((w & (2 * st - 1)) == 0 && w + st < kSpanWarps) {
-                    float bx[SLOTS];
-                    uint32_t bi[SLOTS];
-#pragma unroll
-                    for (int k = 0; k < SLOTS; ++k) {
-                        bx[k] = sh.list_x[par][w + st][lane + 32 * k];
-                        bi[k] = sh.list_i[par][w + st][lane + 32 * k];
-                    }
-                    merge_lists<SLOTS>(sel.L.x, sel.L.id, bx, bi, lane);
-#pragma unroll
-                    for (int k = 0; k < SLOTS; ++k) {
-                        sh.list_x[par][w][lane + 32 * k] = sel.L.x[k];
-                        sh.list_i[par][w][lane + 32 * k] = sel.L.id[k];
-                    }
-                }
-                named_sync(1, kSpanWarps * 32);
-            }
-        } else {
-            named_sync(1, kSpanWarps * 32);
-        }
-        // the merged list is in slot [par][0] and every warp's (C, S) in red_[par]
-        if (w == 0 && lane == 0 && !aborted) mbar_arrive(done0 + 8u * par);
     }
 }
 

@@ -39,21 +39,17 @@ constexpr size_t kQueueDynSmemBudget = 208 * 1024;
 #ifndef LP_PDL
 #define LP_PDL 1  // launch the row kernel as a programmatic dependent of the plan
 #endif
-// Balanced-span kernel: spans of at least this many 16-byte vectors (64 KB) per CTA.
-constexpr uint32_t kSpanMinVec = 4096;
-// (levels 0 | 1..5 | 6) x (warp ranges | row queue | balanced spans) x (plain | extended inputs)
-constexpr int kKinds = 3;
+// (levels 0 | 1..5 | 6) x (warp ranges | row queue) x (plain | extended inputs)
+constexpr int kKinds = 2;
 constexpr int kVariants = 3 * kKinds * 2;
-enum Kind { kWarpRanges = 0, kRowQueue = 1, kSpans = 2 };
+enum Kind { kWarpRanges = 0, kRowQueue = 1 };
 
 struct DeviceInfo {
     bool ready = false;
     bool smem_attr[kVariants] = {};
     int sms = 0;
-    size_t smem_optin = 0;  // shared memory one CTA may use (static + dynamic)
     int occ[kVariants] = {};
     size_t occ_smem[kVariants] = {};
-    size_t static_smem[kVariants] = {};
 };
 
 std::mutex g_mu;
@@ -69,10 +65,7 @@ RowsKernel variant_kernel(int v) {
         case 2: return &lpk::k_rows<2, true, kUnroll, kStages, EXT>;
         case 3: return &lpk::k_rows_cta<1, false, kQU, kQS, kQW, EXT>;
         case 4: return &lpk::k_rows_cta<1, true, kQU, kQS, kQW, EXT>;
-        case 5: return &lpk::k_rows_cta<2, true, kQU, kQS, kQW, EXT>;
-        case 6: return &lpk::k_rows_span<1, false, EXT>;
-        case 7: return &lpk::k_rows_span<1, true, EXT>;
-        default: return &lpk::k_rows_span<2, true, EXT>;
+        default: return &lpk::k_rows_cta<2, true, kQU, kQS, kQW, EXT>;
     }
 }
 
@@ -82,13 +75,7 @@ RowsKernel variant_kernel(int v) {
     return v >= kPerExt ? variant_kernel<true>(v - kPerExt) : variant_kernel<false>(v);
 }
 Kind kind_of(int v) { return (Kind)((v % kPerExt) / 3); }
-int block_threads(int v) {
-    switch (kind_of(v)) {
-        case kRowQueue: return kQW * 32;
-        case kSpans: return lpk::kSpanThreads;
-        default: return lpk::kThreads;
-    }
-}
+int block_threads(int v) { return kind_of(v) == kRowQueue ? kQW * 32 : lpk::kThreads; }
 const void* variant_fn(int v) { return reinterpret_cast<const void*>(variant_kernel(v)); }
 
 int variant_of(uint32_t levels) { return levels == 0 ? 0 : (levels < 6 ? 1 : 2); }
@@ -102,11 +89,7 @@ bool device_info(int* dev_out, DeviceInfo** info) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
             return false;
-        int optin = 0;
-        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || optin <= 0)
-            return false;
         d.sms = sms;
-        d.smem_optin = (size_t)optin;
         d.ready = true;
     }
     *dev_out = dev;
@@ -117,18 +100,7 @@ bool device_info(int* dev_out, DeviceInfo** info) {
 // Allow the variant's largest dynamic shared memory (once per device); false on failure.
 bool set_smem_attr(DeviceInfo* d, int v) {
     if (d->smem_attr[v]) return true;
-    size_t dyn = kMaxDynSmem;
-    if (kind_of(v) == kRowQueue) dyn = kMaxDynSmemQueue;
-    if (kind_of(v) == kSpans) {
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, variant_fn(v)) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return false;
-        }
-        d->static_smem[v] = fa.sharedSizeBytes;
-        if (fa.sharedSizeBytes >= d->smem_optin) return false;
-        dyn = d->smem_optin - fa.sharedSizeBytes;
-    }
+    const size_t dyn = kind_of(v) == kRowQueue ? kMaxDynSmemQueue : kMaxDynSmem;
     if (cudaFuncSetAttribute(variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
@@ -296,9 +268,8 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     p.split_rows = 0;
     p.early = early ? 1u : 0u;
     p.out_rows = out_rows;
-    p.stages = 0;
-    p.next_token = 0;
-    p.drop_chunk = 0xFFFFFFFFu;
+    // next-token logits: one logits row per batch and per position
+    p.next_token = (T == B && T_logits == B && input_row_offsets == nullptr) ? 1u : 0u;
 
     const uint32_t staged_arrays = (p.loff != p.off) ? 3u : 2u;
     const size_t smem =
@@ -313,46 +284,13 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     int occ = occupancy(d, v, smem);
     if (occ == 0) return LP_ERR_CUDA;
     uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;  // occ <= kMaxCtasPerSm
-    const char* force = std::getenv("LP_RAGGED_KERNEL");  // test hook: "warp", "queue" or "span"
+    const char* force = std::getenv("LP_RAGGED_KERNEL");  // test hook: "warp" or "queue"
     const uint32_t r_max = T < T_logits ? T : T_logits;
-    Kind kind = r_max <= 3u * (uint32_t)d->sms ? kRowQueue : kWarpRanges;
-    if (force && std::strcmp(force, "warp") == 0) kind = kWarpRanges;
-    if (force && std::strcmp(force, "queue") == 0) kind = kRowQueue;
-    if (force && std::strcmp(force, "span") == 0) kind = kSpans;
-    const bool queue = kind == kRowQueue;
+    bool queue = r_max <= 3u * (uint32_t)d->sms;
+    if (force && std::strcmp(force, "warp") == 0) queue = false;
+    if (force && std::strcmp(force, "queue") == 0) queue = true;
     size_t launch_smem = smem;
     unsigned block = lpk::kThreads;
-    if (kind == kSpans) {
-        // One CTA per SM; as many 32 KB ring stages as fit beside the staged batch arrays.
-        v += 3 * kSpans;
-        {
-            std::lock_guard<std::mutex> lock(g_mu);
-            if (!set_smem_attr(d, v)) return LP_ERR_CUDA;
-        }
-        const size_t dyn_max = d->smem_optin - d->static_smem[v];
-        // next-token logits: one logits row per batch and per position (no batch arrays read)
-        p.next_token = (T == B && T_logits == B && input_row_offsets == nullptr) ? 1u : 0u;
-        if (p.next_token) p.stage_offsets = 0;
-        size_t staged = p.stage_offsets ? smem - kRingBytes : 0;
-        uint32_t ns = (uint32_t)((dyn_max - staged) / lpk::kSpanChunkBytes);
-        if (ns < 4 && staged) {  // many batches: read the offsets from global memory instead
-            p.stage_offsets = 0;
-            staged = 0;
-            ns = (uint32_t)(dyn_max / lpk::kSpanChunkBytes);
-        }
-        if (ns > lpk::kSpanMaxStages) ns = lpk::kSpanMaxStages;
-        if (ns < 2) return LP_ERR_CUDA;
-        p.stages = ns;
-        p.min_piece = kSpanMinVec;
-        const char* fm = std::getenv("LP_RAGGED_SPAN_MIN");  // test hook: vectors per span at least
-        if (fm) p.min_piece = (uint32_t)std::strtoul(fm, nullptr, 10);
-        if (p.min_piece < 1) p.min_piece = 1;
-        const char* fd = std::getenv("LP_RAGGED_TEST_DROP_CHUNK");  // test hook: the bounded waits
-        if (fd) p.drop_chunk = (uint32_t)std::strtoul(fd, nullptr, 10);
-        launch_smem = (size_t)ns * lpk::kSpanChunkBytes + staged;
-        grid = (uint32_t)d->sms;
-        block = lpk::kSpanThreads;
-    }
     if (queue) {
         v += 3 * kRowQueue;
         block = kQW * 32;
@@ -529,7 +467,6 @@ const char* lp_ragged_strerror(lp_status status) {
         case LP_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case LP_ERR_CUDA: return "CUDA launch or copy failed";
         case LP_ERR_TEMPERATURE: return "a temperature is not a positive finite number";
-        case LP_ERR_TIMEOUT: return "a device-side copy wait gave up (the kernel wrote no further rows)";
         default: return "unknown lp_status";
     }
 }

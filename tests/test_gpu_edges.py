@@ -155,7 +155,7 @@ def test_bad_offsets_detected_on_device():
                             torch.zeros(3, dtype=torch.int32, device="cuda"), echo, 3)
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 @pytest.mark.parametrize("name,kw", [("decode", dict(B=40)), ("prefill", dict(B=3, max_len=90)),
                                      ("mixed", dict(B=9, max_len=20)), ("wide", dict(B=2, max_len=12)),
                                      ("tiny", dict())])
@@ -165,7 +165,7 @@ def test_both_kernels(kernel, name, kw, monkeypatch):
     parity.check_batch(workloads.make_batch(name, "cuda", **kw), what=f"{name}/{kernel}")
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 def test_both_kernels_edge_rows(kernel, monkeypatch):
     monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
     g = torch.Generator().manual_seed(11)
@@ -180,7 +180,7 @@ def test_both_kernels_edge_rows(kernel, monkeypatch):
     assert np.array_equal(first[2], again[2]) and np.array_equal(first[1], again[1], equal_nan=True)
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 @pytest.mark.parametrize("levels", [1, 2, 3])
 def test_top_elements_in_one_lane(kernel, levels, monkeypatch):
     # Rows whose top-k sits in few lanes' elements or is decided by ties: all-equal rows,
@@ -210,7 +210,7 @@ def test_top_elements_in_one_lane_misaligned(V):
     parity.check_batch(_custom(x, [6], [1], 3, seed=V), what=f"one-lane-misaligned/{V}")
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 def test_compute_twice_after_one_plan(kernel, monkeypatch):
     # The row kernels leave their queue and ticket words cleared, so a second compute on
     # the same plan (no plan in between) gives the same rows, bit for bit (both kernels
@@ -264,7 +264,7 @@ def test_kernel_choice_boundary(B, V):
     parity.check_batch(b, rows=parity.sample_rows(B, 40, seed=B), what=f"B={B} V={V}")
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 @pytest.mark.parametrize("quantised", [False, True])
 def test_levels5_long_rows(kernel, quantised, monkeypatch):
     # top-31 over long rows: the row queue bounds it by the 16th largest of each lane
@@ -279,7 +279,7 @@ def test_levels5_long_rows(kernel, quantised, monkeypatch):
     parity.check_batch(b, what=f"levels 5/{kernel}/{'quantised' if quantised else 'normal'}")
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 @pytest.mark.parametrize("B", [1025, 2047])
 def test_many_batches_staged_row_lookup(kernel, B, monkeypatch):
     # Up to 2047 batches the offsets sit in shared memory and a row's batch is found with two
@@ -300,7 +300,7 @@ def test_decode_full_size_levels6_sampled():
     parity.check_batch(b, rows=parity.sample_rows(b.B, 16, seed=6), what="decode levels 6")
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 def test_levels6_quantised_ties(kernel, monkeypatch):
     # The top-63 bound compares with >= against a real element's value: elements equal to
     # it must still reach the candidates (many exact ties).
@@ -310,49 +310,3 @@ def test_levels6_quantised_ties(kernel, monkeypatch):
     b = workloads.make_custom_batch(x, [1] * 9, [0] * 9, 6, seed=14)
     parity.check_batch(b, what=f"levels 6 ties/{kernel}")
 
-
-@pytest.mark.parametrize("span_min", [1, 33, 300])
-@pytest.mark.parametrize("B,V,levels", [(1, 128256, 3), (5, 20011, 6), (13, 111, 3), (40, 50000, 0), (3, 9999, 1),
-                                        (256, 128256, 3)])
-def test_span_pieces(span_min, B, V, levels, monkeypatch):
-    # Balanced-span kernel with spans of at least `span_min` vectors: rows cut by span ends
-    # into many pieces (down to pieces that hold only a row's partial edge vector, and CTAs
-    # whose span crosses several rows), merged by the CTA that takes the row's last ticket.
-    monkeypatch.setenv("LP_RAGGED_KERNEL", "span")
-    monkeypatch.setenv("LP_RAGGED_SPAN_MIN", str(span_min))
-    b = workloads.make_next_token_batch(B, V, levels=levels, dist="normal", scale=3.0, device="cuda",
-                                        seed=B * 37 + span_min)
-    rows = None if B * V <= 40 * 50000 else parity.sample_rows(B, 40, seed=span_min)
-    parity.check_batch(b, rows=rows, what=f"span_min={span_min} B={B} V={V} levels={levels}")
-
-
-@pytest.mark.parametrize("span_min", [7, 500])
-def test_span_pieces_echo_and_variants(span_min, monkeypatch):
-    monkeypatch.setenv("LP_RAGGED_KERNEL", "span")
-    monkeypatch.setenv("LP_RAGGED_SPAN_MIN", str(span_min))
-    b = workloads.make_batch("mixed", "cuda", B=6, max_len=9, V=30011, seed=70 + span_min)
-    parity.check_batch(b, what=f"mixed span_min={span_min}")
-    bv = workloads.with_temperatures(workloads.make_batch("mixed", "cuda", B=6, max_len=9, V=30011,
-                                                          variable_extra=2, seed=71), seed=span_min)
-    parity.check_batch(bv, what=f"variable+tau span_min={span_min}")
-    bt = workloads.with_temperatures(workloads.make_next_token_batch(9, 40003, levels=3, device="cuda", seed=72),
-                                     seed=span_min)
-    parity.check_batch(bt, what=f"next-token+tau span_min={span_min}")
-
-
-def test_span_bounded_wait_gives_up(monkeypatch):
-    # A copy that never arrives (test hook: each CTA leaves its third chunk unissued): the
-    # waits on it give up after their time limit, the launch sets LP_ERR_TIMEOUT, and the
-    # context stays usable (the next launch on the same workspace is exact).
-    monkeypatch.setenv("LP_RAGGED_KERNEL", "span")
-    b = workloads.make_next_token_batch(64, 128256, levels=3, device="cuda", seed=5)
-    ws = lp.new_workspace(b.B, b.T, b.V, b.levels)
-    out_off = lp.plan(b.logit_row_offsets, b.echo, b.T, ws)
-    out_lp = torch.empty((b.B, 8), device="cuda")
-    out_tok = torch.empty((b.B, 8), dtype=torch.int32, device="cuda")
-    monkeypatch.setenv("LP_RAGGED_TEST_DROP_CHUNK", "2")
-    lp.compute(b.logits, b.logit_row_offsets, b.tokens, b.sampled_tokens, out_off, b.echo, 3, out_lp, out_tok, ws)
-    torch.cuda.synchronize()
-    assert lp.read_status(ws) & (1 << 9)
-    monkeypatch.delenv("LP_RAGGED_TEST_DROP_CHUNK")
-    parity.check_batch(b, what="after a launch that gave up")

@@ -48,7 +48,7 @@ def check_equal(b, what):
     assert np.array_equal(g_lp[:R], r_lp, equal_nan=True), what
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 @pytest.mark.parametrize("name,kw", [("decode", dict(B=40)), ("prefill", dict(B=3, max_len=90)),
                                      ("mixed", dict(B=9, max_len=20)), ("wide", dict(B=2, max_len=12)),
                                      ("tiny", dict())])
@@ -57,7 +57,7 @@ def test_step_equals_plan_and_compute(kernel, name, kw, monkeypatch):
     check_equal(workloads.make_batch(name, "cuda", **kw), f"{name}/{kernel}")
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 def test_step_variants_and_split_rows(kernel, monkeypatch):
     monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
     b = workloads.make_batch("mixed", "cuda", B=10, max_len=16, V=30011, variable_extra=2, seed=81)
@@ -110,7 +110,7 @@ def test_step_reports_the_reduction_status():
     assert np.isnan(g_lp[1, 7]) and g_tok[1, 7] == 600
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 def test_step_repeated_then_compute(kernel, monkeypatch):
     # Steps and a plain compute on one workspace: the counters the row kernels use are
     # back to zero after each launch, so every call gives the same rows.

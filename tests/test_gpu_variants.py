@@ -19,7 +19,7 @@ def _built():
     parity.ensure_built()
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 @pytest.mark.parametrize("levels", [0, 1, 3, 5, 6])
 def test_temperature_every_levels(kernel, levels, monkeypatch):
     monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)
@@ -27,7 +27,7 @@ def test_temperature_every_levels(kernel, levels, monkeypatch):
     parity.check_batch(workloads.with_temperatures(b, seed=levels), what=f"tau/{kernel}/{levels}")
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 @pytest.mark.parametrize("name,kw", [("decode", dict(B=24)), ("prefill", dict(B=3, max_len=80)),
                                      ("wide", dict(B=2, max_len=10)), ("tiny", dict())])
 def test_variable_logits_workloads(kernel, name, kw, monkeypatch):
@@ -37,7 +37,7 @@ def test_variable_logits_workloads(kernel, name, kw, monkeypatch):
     parity.check_batch(workloads.with_temperatures(b, seed=2), what=f"variable+tau/{name}/{kernel}")
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 def test_variable_mixed_echo_and_extra_rows(kernel, monkeypatch):
     # Non-echo batches with 1-4 present rows (only the last is read), echo batches with all.
     monkeypatch.setenv("LP_RAGGED_KERNEL", kernel)

@@ -63,7 +63,7 @@ def check_sharded(b, bounds, what):
     assert np.array_equal(g_tok, u_tok), f"{what}: ids differ from the unsharded path"
 
 
-@pytest.mark.parametrize("kernel", ["warp", "queue", "span"])
+@pytest.mark.parametrize("kernel", ["warp", "queue"])
 @pytest.mark.parametrize("name,kw,P", [
     ("decode", dict(B=24), 8),
     ("decode", dict(B=5), 1),
