@@ -83,9 +83,11 @@ constexpr uint32_t kStatusTemperature = 1u << 8; // bit of LP_ERR_TEMPERATURE
 // Workspace: [header 256 B][arrival counters u32 x max warps, zeroed by plan, padded
 // to 256 B][partial slots].
 struct WsHeader {
-    uint32_t status;
+    uint32_t status;       // status bits of the plan and of every launch after it
     uint32_t rows;
-    uint32_t reserved[62];
+    uint32_t plan_status;  // the plan's own bits: no row kernel writes it, so every CTA of a
+                           // launch reads the same value whatever the others have flagged
+    uint32_t reserved[61];
 };
 
 // Partial tuple of one piece of a split row (u32 words):
@@ -105,6 +107,7 @@ struct RowsParams {
     float* out_lp;
     uint32_t* out_tok;
     uint32_t* status;
+    const uint32_t* plan_status;  // the plan's bits alone (WsHeader::plan_status)
     uint32_t* counters;      // per split row (indexed by its first warp): pieces arrived
     unsigned char* partials;
     uint32_t T, V, B, K, W;
@@ -199,6 +202,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(const uint32_t* __restric
         if (out_off != nullptr) out_off[B] = s_carry;
         hdr->rows = s_carry;
         hdr->status = s_bad ? kStatusOffsets : 0u;
+        hdr->plan_status = s_bad ? kStatusOffsets : 0u;
     }
 }
 
@@ -410,6 +414,16 @@ __device__ __forceinline__ float4 load_checked(const float* rowp, const float* v
 __device__ __forceinline__ bool refresh_due(uint32_t blk) {
     return (blk & (kThrEvery - 1)) == 0 || (blk < kThrEvery && (blk & (blk - 1)) == 0);
 }
+#ifndef LP_Q_REFRESH
+#define LP_Q_REFRESH 1  // row-queue refresh schedule for K <= 7: blocks 0, 4, 8, then every 8
+#endif
+// Refreshes of the row-queue warps (a CTA-wide table of lane maxima) for K <= 7.
+__device__ __forceinline__ bool refresh_due_q(uint32_t blk, int w) {
+    if (LP_Q_REFRESH == 1) return (blk & 3u) == 0 && (blk <= 8u || (blk & 7u) == 0);
+    if (LP_Q_REFRESH == 2) return blk == 0 || blk == 2 || (blk & 7u) == 4u;
+    if (LP_Q_REFRESH == 3) return blk == 0 || blk == 2 || blk == 4 || (blk >= 8u && ((blk + (uint32_t)w) & 7u) == 0);
+    return refresh_due(blk);
+}
 
 // Candidate mask of one block: bit 4u+k set when element k of vector u is >= thr.
 template <int U>
@@ -445,7 +459,7 @@ __device__ __forceinline__ void select_block(const float4 (&v)[U], float bm, uin
         // threshold that follows the warp's true K-th best at the cost of one float
         // sort, refreshed on blocks 0, 1, 2 and 4 (it rises fastest early) and then
         // every kThrEvery blocks.
-        if (refresh_due(blk)) {
+        if ((TABW > 0 && sel.K <= 7u) ? refresh_due_q(blk, w) : refresh_due(blk)) {
             float lm = ls.m;
             uint32_t kk = sel.K;
             if constexpr (TABW > 0) {
@@ -1042,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
     } else {
         pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
         // Status, row count and the offsets are fetched in one round trip.
-        status = __ldcg(p.status);
+        status = __ldcg(p.plan_status);
         R = __ldcg(p.out_off + B);
         if (p.stage_offsets) {
             stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kThreads, off, loff, out_off, echo);
@@ -1232,7 +1246,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         status = 0u;
         R = B;
         if (threadIdx.x == 0) {
-            cp_async4((uint32_t)__cvta_generic_to_shared(&cm.status), p.status);
+            cp_async4((uint32_t)__cvta_generic_to_shared(&cm.status), p.plan_status);
             cp_async4((uint32_t)__cvta_generic_to_shared(&cm.rows), out_off + B);
         }
     } else {
@@ -1240,7 +1254,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         // one read for the whole CTA: other CTAs may set status bits meanwhile, and every
         // thread must leave the task loop below on the same task count
         if (threadIdx.x == 0) {
-            cm.status = __ldcg(p.status);
+            cm.status = __ldcg(p.plan_status);
             cm.rows = __ldcg(p.out_off + B);
         }
         if (p.stage_offsets) stage_batch_arrays<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo);
@@ -1252,9 +1266,9 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     // Tasks: piece `task % S` of row `task / S` (S = p.split pieces per row). The launch
     // holds two CTAs per SM and the first min(tasks, SMs) CTAs (one per SM in the
     // hardware's dispatch order) start on task blockIdx.x without an atomic; every later
-    // task comes from a queue: [0] next task of [nA, R*S), [1] CTAs finished; with S > 1,
-    // one arrival ticket per row from [2]. Any CTA may take any task, so the result does
-    // not depend on where CTAs land, only the balance does.
+    // task comes from a queue: [0] next task of [nA, R*S) ([1] unused); with S > 1, one
+    // arrival ticket per row from [2]. Any CTA may take any task, so the result does not
+    // depend on where CTAs land, only the balance does.
     const uint32_t S = p.split;
     uint32_t* queue = p.counters;
     uint32_t* tickets = queue + 2;
@@ -1265,8 +1279,16 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const uint32_t nA = ntask < p.num_sms ? ntask : p.num_sms;
     // A CTA without a task of its own goes to the queue (counters): after the plan.
     if (early && blockIdx.x >= nA) pdl_wait();
+    // Every CTA asks the queue after each task (and a CTA without a task of its own once at
+    // its start) until it is told there is none: one request per queued task, one refusal
+    // per CTA that asks. Every CTA sees the same task count, so the number of requests is
+    // known, and the request that comes last resets the queue for the next call (no CTA
+    // touches it afterwards), so no CTA has to count itself out at its end.
+    const uint32_t requests = ntask > nA ? ntask - nA + gridDim.x : nA;
     auto next_task = [&]() -> uint32_t {  // thread 0 only
-        const uint32_t rb = nA + atomicAdd(queue, 1u);
+        const uint32_t r = atomicAdd(queue, 1u);
+        if (r == requests - 1u) queue[0] = 0u;
+        const uint32_t rb = nA + r;
         return rb < ntask ? rb : ntask;
     };
     if (threadIdx.x == 0) {
@@ -1352,8 +1374,6 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         const float* rowp = d.rowp;
         const uint32_t pq0 = S == 1u ? 0u : (uint32_t)(((uint64_t)p.nq * piece) / S);
         const uint32_t pq1 = S == 1u ? p.nq : (uint32_t)(((uint64_t)p.nq * (piece + 1)) / S);
-        const uint32_t wq0 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * w) / NW);
-        const uint32_t wq1 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * (w + 1)) / NW);
         bool t_here;
 
         LaneSum ls;
@@ -1361,6 +1381,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         Selector<SLOTS> sel;
         sel.init(s_cx[w], s_ci[w], K);
         float xt = 0.f;
+        const uint32_t wq0 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * w) / NW);
+        const uint32_t wq1 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * (w + 1)) / NW);
         stream_piece<SLOTS, TOPK, U, STAGES, NW>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr,
                                                  &cm.lane_max[0][0], w);
         if (early) pdl_wait();  // the plan has finished before the queue, tickets or status are touched
@@ -1477,15 +1499,6 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                 }
             }
             __syncthreads();
-        }
-    }
-    if (early) pdl_wait();
-    // No fence before the count: this CTA's queue requests have all returned, and nothing
-    // it wrote is read again in this launch (the next call sees it after the kernel ends).
-    if (threadIdx.x == 0) {
-        if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {  // last CTA out: ready for the next call
-            queue[0] = 0u;
-            queue[1] = 0u;
         }
     }
 }

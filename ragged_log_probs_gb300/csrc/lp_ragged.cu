@@ -250,6 +250,7 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     p.out_lp = out_logprobs;
     p.out_tok = out_tokens;
     p.status = &reinterpret_cast<lpk::WsHeader*>(ws)->status;
+    p.plan_status = &reinterpret_cast<lpk::WsHeader*>(ws)->plan_status;
     p.counters = reinterpret_cast<uint32_t*>(ws + sizeof(lpk::WsHeader));
     p.partials = ws + sizeof(lpk::WsHeader) + counters_bytes(g_max);
     p.T = T;
