@@ -56,6 +56,9 @@ namespace lpk {
 #ifndef LP_NEXT_TOKEN_FAST
 #define LP_NEXT_TOKEN_FAST 1  // row queue: next-token compute launches stream before reading offsets
 #endif
+#ifndef LP_PREFETCH_BEFORE_WAIT
+#define LP_PREFETCH_BEFORE_WAIT 1  // row queue, next-token compute launches: L2 prefetch before the wait
+#endif
 #ifndef LP_EARLY_TRIGGER
 #define LP_EARLY_TRIGGER 1  // row kernels let their programmatic dependents launch at once
 #endif
@@ -1238,6 +1241,12 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         stage_and_scan<EXT>(p, s_dyn, threadIdx.x, kT, off, loff, out_off, echo, R, bad);
         status = bad ? kStatusOffsets : 0u;
     } else if (fast) {
+        // An L2 prefetch of the CTA's first task is a hint with no effect on any result, so it
+        // may come before the dependency wait: should an earlier kernel still write these
+        // logits, its writes update the lines in L2 (the point of coherence); when this
+        // launch's CTAs become resident during the previous launch's tail, HBM serves them
+        // meanwhile.
+        if (LP_PREFETCH_BEFORE_WAIT && lane == 0) prefetch_own_task<NW>(p, w);
         pdl_wait();  // plan's outputs (status, output offsets, cleared counters) are visible
         // Next-token logits: the tasks are known without the offsets (see
         // RowsParams::next_token). The plan's status and the caller's row count arrive in
