@@ -166,7 +166,11 @@ lp_status lp_ragged_compute_ex(const float *logits, uint32_t T_logits, uint32_t 
  * it streams the logits while the plan is still running (it derives the output rows
  * from the offsets itself, with the plan's checks) and waits for the plan only before
  * it touches the workspace counters or the status word; the rows are identical to
- * lp_ragged_plan + lp_ragged_compute_ex.
+ * lp_ragged_plan + lp_ragged_compute_ex. With next-token logits (T == B == T_logits,
+ * input_row_offsets NULL) the plan itself starts on the device as soon as the previous
+ * kernel on the stream has finished (no launch gap; it waits for that kernel before it
+ * reads or writes anything), and the reduction streams row o from logits row o before
+ * it reads any offset; a layout the plan rejects still writes no row.
  *   output_row_offsets   device out, uint32[B+1] (as lp_ragged_plan)
  *   host_rows_and_status pinned host out, uint32[2] or NULL: {R, status}, copied after
  *                        the reduction (so the status holds the plan's and the

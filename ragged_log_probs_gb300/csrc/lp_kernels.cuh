@@ -162,6 +162,11 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(const uint32_t* __restric
     __shared__ uint32_t s_warp[kPlanThreads / 32];
     __shared__ uint32_t s_carry;
     __shared__ uint32_t s_bad;
+    // Launched as a programmatic dependent (a next-token step): everything earlier on the
+    // stream has finished, the previous row kernel's use of the counters included, before
+    // the inputs are read or anything is written (a no-op for an ordinary launch). Only then
+    // may the row kernel launch: it reads the logits before it waits for this plan.
+    pdl_wait();
     pdl_launch_dependents();  // the row kernel may launch now; it waits for our writes
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     if (tid == 0) { s_carry = 0; s_bad = 0; }
@@ -1230,10 +1235,17 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const uint32_t* loff = p.loff;
     const uint32_t* out_off = p.out_off;
     const uint8_t* echo = p.echo;
-    const bool early = p.early && p.stage_offsets;
-    const bool fast = LP_NEXT_TOKEN_FAST && p.next_token != 0u && !p.early;
+    const bool fast = LP_NEXT_TOKEN_FAST && p.next_token != 0u;
+    const bool early = p.early && (fast || p.stage_offsets);
     uint32_t status, R;
-    if (early) {
+    if (fast && early) {
+        // A step on next-token logits: the plan, which let this launch start only once all
+        // earlier work had finished, may still be running; the tasks are known without the
+        // offsets (see RowsParams::next_token), so the first rows stream at once. The plan's
+        // status and the row offsets are read after the stream's wait for the plan.
+        status = 0u;
+        R = B;
+    } else if (early) {
         // The logits are complete (the plan, launched after all earlier work, is running).
         if (p.T_logits == B && lane == 0) prefetch_own_task<NW>(p, w);
         // rows derived here: the plan may still be running (see RowsParams::early)
@@ -1286,6 +1298,14 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const bool bad = (status & kStatusOffsets) || too_many;
     const uint32_t ntask = bad ? 0u : R * S;
     const uint32_t nA = ntask < p.num_sms ? ntask : p.num_sms;
+    // Task -> row o, piece of the row, pieces of the row, partial slot of its piece 0.
+    struct TaskRef {
+        uint32_t o, piece, n, slot0;
+    };
+    auto task_ref = [&](uint32_t task) -> TaskRef {
+        const uint32_t oo = S == 1u ? task : task / S;
+        return TaskRef{oo, task - oo * S, S, oo * S};
+    };
     // A CTA without a task of its own goes to the queue (counters): after the plan.
     if (early && blockIdx.x >= nA) pdl_wait();
     // Every CTA asks the queue after each task (and a CTA without a task of its own once at
@@ -1349,7 +1369,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     for (;;) {
         const uint32_t task = cm.row;
         if (task >= ntask) break;
-        const uint32_t o = S == 1u ? task : task / S, piece = task - o * S;
+        const TaskRef tr = task_ref(task);
+        const uint32_t o = tr.o, piece = tr.piece, Sr = tr.n;
         RowDesc d;
         if (fast) {
             d.rowp = p.logits + (size_t)o * V;
@@ -1361,7 +1382,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                 d.tau = p.tau[o];
                 d.k = __fdiv_rn(kLog2e, d.tau);
             }
-            if (threadIdx.x == 0) {  // the caller's output offsets of row o, fetched meanwhile
+            if (threadIdx.x == 0 && !early) {  // the caller's output offsets of row o, fetched meanwhile
                 cp_async4((uint32_t)__cvta_generic_to_shared(&cm.chk[0]), out_off + o);
                 cp_async4((uint32_t)__cvta_generic_to_shared(&cm.chk[1]), out_off + o + 1);
                 cp_async_commit();
@@ -1381,8 +1402,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         const uint32_t t = d.t;
         const uint32_t t_loc = EXT ? t - p.vocab_base : t;  // column of the target in this shard
         const float* rowp = d.rowp;
-        const uint32_t pq0 = S == 1u ? 0u : (uint32_t)(((uint64_t)p.nq * piece) / S);
-        const uint32_t pq1 = S == 1u ? p.nq : (uint32_t)(((uint64_t)p.nq * (piece + 1)) / S);
+        const uint32_t pq0 = Sr == 1u ? 0u : (uint32_t)(((uint64_t)p.nq * piece) / Sr);
+        const uint32_t pq1 = Sr == 1u ? p.nq : (uint32_t)(((uint64_t)p.nq * (piece + 1)) / Sr);
         bool t_here;
 
         LaneSum ls;
@@ -1395,6 +1416,16 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         stream_piece<SLOTS, TOPK, U, STAGES, NW>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr,
                                                  &cm.lane_max[0][0], w);
         if (early) pdl_wait();  // the plan has finished before the queue, tickets or status are touched
+        if (fast && early && threadIdx.x == 0) {
+            // the plan's outputs this task's checks need, read during the merges below
+            if (cm.fast_ok == 2u) {
+                cp_async4((uint32_t)__cvta_generic_to_shared(&cm.status), p.plan_status);
+                cp_async4((uint32_t)__cvta_generic_to_shared(&cm.rows), out_off + B);
+            }
+            cp_async4((uint32_t)__cvta_generic_to_shared(&cm.chk[0]), out_off + o);
+            cp_async4((uint32_t)__cvta_generic_to_shared(&cm.chk[1]), out_off + o + 1);
+            cp_async_commit();
+        }
         // The CTA's next task is asked for now, so the round trip overlaps the merges.
         uint32_t next = 0;
         if (threadIdx.x == 0) next = next_task();
@@ -1440,7 +1471,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                 // a layout the plan rejects: nothing written, nothing published
             } else if (row_err) {
                 if (piece == 0) emit_invalid<EXT>(p, o, row_err, lane);
-            } else if (S == 1) {
+            } else if (Sr == 1) {
                 if (EXT && p.tuple_out != nullptr)
                     store_row_tuple<SLOTS, TOPK>(p, o, sel.L, C, Sm, t, cm.has_xt != 0, cm.xt, lane);
                 else
@@ -1449,9 +1480,9 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                 // a piece of a split row: publish it; the CTA that takes the row's last
                 // ticket merges all pieces
                 store_piece<SLOTS, TOPK>(
-                    reinterpret_cast<uint32_t*>(p.partials + (size_t)(o * S + piece) * p.stride), K, sel.L, C, Sm,
-                    cm.has_xt != 0, cm.xt, lane);
-                last = take_ticket(tickets, o, S, lane) ? 1u : 0u;
+                    reinterpret_cast<uint32_t*>(p.partials + (size_t)(tr.slot0 + piece) * p.stride), K, sel.L, C,
+                    Sm, cm.has_xt != 0, cm.xt, lane);
+                last = take_ticket(tickets, o, Sr, lane) ? 1u : 0u;
             }
             __syncwarp();
             if (lane == 0) {
@@ -1463,14 +1494,14 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         }
         cm.lane_max[w][lane] = neg_inf();  // every warp is past this task's stream
         __syncthreads();
-        if (S > 1 && cm.last) {
-            // ---- merge the row's S pieces with the whole CTA -----------------------------
-            const unsigned char* base = p.partials + (size_t)o * S * p.stride;
+        if (Sr > 1 && cm.last) {
+            // ---- merge the row's Sr pieces with the whole CTA ----------------------------
+            const unsigned char* base = p.partials + (size_t)tr.slot0 * p.stride;
             C = neg_inf();
             Sm = 0.f;
             bool has = false;
             float xr = 0.f;
-            for (uint32_t j = threadIdx.x; j < S; j += kT) {
+            for (uint32_t j = threadIdx.x; j < Sr; j += kT) {
                 const uint32_t* hw = reinterpret_cast<const uint32_t*>(base + (size_t)j * p.stride);
                 lse2_combine(C, Sm, __uint_as_float(__ldcg(hw)), __uint_as_float(__ldcg(hw + 1)));
                 if (__ldcg(hw + 3)) { xr = __uint_as_float(__ldcg(hw + 2)); has = true; }
@@ -1483,7 +1514,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
             if (has) { cm.xt = xr; cm.has_xt = 1u; }  // one piece holds the target
             sel.L.reset();
             if constexpr (TOPK) {
-                for (uint32_t j = (uint32_t)w; j < S; j += NW) {
+                for (uint32_t j = (uint32_t)w; j < Sr; j += NW) {
                     float cx[SLOTS];
                     uint32_t ci[SLOTS];
                     load_piece_list<SLOTS>(reinterpret_cast<const uint32_t*>(base + (size_t)j * p.stride), K, lane,

@@ -156,7 +156,7 @@ size_t lp_ragged_workspace_size(uint32_t B, uint32_t T, uint32_t V, uint32_t lev
 // it checks the offsets, counts the rows and clears the status word and counters.
 static lp_status plan_launch(const uint32_t* logit_row_offsets, const uint8_t* echo, uint32_t B, uint32_t T,
                              uint32_t* output_row_offsets, void* workspace, size_t workspace_bytes,
-                             cudaStream_t s, bool validate_only = false) {
+                             cudaStream_t s, bool validate_only = false, bool programmatic = false) {
     if (!logit_row_offsets || !echo || (!output_row_offsets && !validate_only)) return LP_ERR_NULL;
     if (!workspace) return LP_ERR_WORKSPACE;
     if (B == 0 || T == 0) return LP_ERR_SHAPE;
@@ -168,8 +168,26 @@ static lp_status plan_launch(const uint32_t* logit_row_offsets, const uint8_t* e
     if (workspace_bytes < sizeof(lpk::WsHeader) + counters_bytes(g_max)) return LP_ERR_WORKSPACE;
     auto* hdr = static_cast<lpk::WsHeader*>(workspace);
     auto* counters = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) + sizeof(lpk::WsHeader));
-    lpk::k_plan<<<1, lpk::kPlanThreads, 0, s>>>(logit_row_offsets, echo, B, T,
-                                               validate_only ? nullptr : output_row_offsets, hdr, counters, g_max);
+    uint32_t* oo = validate_only ? nullptr : output_row_offsets;
+    if (!programmatic) {
+        lpk::k_plan<<<1, lpk::kPlanThreads, 0, s>>>(logit_row_offsets, echo, B, T, oo, hdr, counters, g_max);
+    } else {
+        // a programmatic dependent of the previous kernel: k_plan waits for it on the device
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(lpk::kPlanThreads);
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, lpk::k_plan, logit_row_offsets, echo, B, T, oo, hdr, counters, g_max) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return LP_ERR_CUDA;
+        }
+    }
     if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return LP_ERR_CUDA; }
     return LP_OK;
 }
@@ -374,10 +392,15 @@ lp_status lp_ragged_step(const float* logits, uint32_t T_logits, uint32_t V, con
                                          nullptr, workspace, workspace_bytes, &d);
     if (chk != LP_OK) return chk;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // The plan is an ordinary launch (after everything before it on the stream); the row
-    // kernel follows it directly, so it may read its inputs before the plan has finished.
+    // The reduction directly follows the plan and reads its inputs before the plan has
+    // finished: the plan lets it launch only once everything earlier on the stream is done.
+    // On next-token logits (one logits row per batch and per position) the plan is itself a
+    // programmatic dependent of the previous kernel (it waits for it on the device, so no
+    // launch gap) and the reduction streams without reading the offsets first; otherwise
+    // the plan is an ordinary launch.
+    const bool next_token = T == B && T_logits == B && input_row_offsets == nullptr;
     lp_status st = plan_launch(input_row_offsets ? input_row_offsets : logit_row_offsets, echo, B, T,
-                               output_row_offsets, workspace, workspace_bytes, s);
+                               output_row_offsets, workspace, workspace_bytes, s, false, next_token);
     if (st != LP_OK) return st;
     st = compute_impl(logits, T_logits, V, logit_row_offsets, input_row_offsets, T, B, tokens, sampled_tokens,
                       output_row_offsets, echo, temperatures, levels, out_logprobs, out_tokens, nullptr, 0u, 0u,
