@@ -200,6 +200,26 @@ __device__ __forceinline__ void merge_lists(float (&ax)[SLOTS], uint32_t (&ai)[S
     }
 }
 
+// a := best N of (a U b) for lists sorted descending in lanes 0..N-1 (N = 8, 16 or 32;
+// the lanes of each other group of N work on their own entries, which nothing reads): the
+// larger of a[l] and b[N-1-l] form a bitonic sequence holding the best N, which log2(N)
+// half-cleaner stages sort.
+template <int N>
+__device__ __forceinline__ void merge_top(float& ax, uint32_t& ai, float bx, uint32_t bi, int lane) {
+    static_assert(N == 8 || N == 16 || N == 32, "group of 8, 16 or 32 lanes");
+    const int src = (lane & ~(N - 1)) | ((N - 1) - (lane & (N - 1)));
+    const float rx = __shfl_sync(kFull, bx, src);
+    const uint32_t ri = __shfl_sync(kFull, bi, src);
+    if (better(rx, ri, ax, ai)) { ax = rx; ai = ri; }
+#pragma unroll
+    for (int j = N / 2; j > 0; j >>= 1) {
+        const float ox = __shfl_xor_sync(kFull, ax, j);
+        const uint32_t oid = __shfl_xor_sync(kFull, ai, j);
+        const bool lower = (lane & j) == 0;
+        if (better(ox, oid, ax, ai) == lower) { ax = ox; ai = oid; }
+    }
+}
+
 // Packed fp32 pair arithmetic (one instruction for two lanes of data, sm_100+).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     float2 d;

@@ -1334,6 +1334,9 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     __syncthreads();
 
     // The warps' sorted lists (in cm.list_*) merged into warp 0's list by a shared-memory tree.
+    // Only the first K entries are read after the merge, so with one slot per lane the tree
+    // merges the first 8 or 16 entries when K fits (fewer stages per round).
+    const int tree_width = K <= 8u ? 8 : (K <= 16u ? 16 : 32);
     auto tree_merge = [&](WarpList<SLOTS>& L) {
         if constexpr (TOPK) {
 #pragma unroll
@@ -1354,7 +1357,13 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                         bx[k] = cm.list_x[w + st][lane + 32 * k];
                         bi[k] = cm.list_i[w + st][lane + 32 * k];
                     }
-                    merge_lists<SLOTS>(L.x, L.id, bx, bi, lane);
+                    if constexpr (SLOTS == 1) {
+                        if (tree_width == 8) merge_top<8>(L.x[0], L.id[0], bx[0], bi[0], lane);
+                        else if (tree_width == 16) merge_top<16>(L.x[0], L.id[0], bx[0], bi[0], lane);
+                        else merge_top<32>(L.x[0], L.id[0], bx[0], bi[0], lane);
+                    } else {
+                        merge_lists<SLOTS>(L.x, L.id, bx, bi, lane);
+                    }
 #pragma unroll
                     for (int k = 0; k < SLOTS; ++k) {
                         cm.list_x[w][lane + 32 * k] = L.x[k];
