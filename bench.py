@@ -57,9 +57,14 @@ PER_CONFIG = ("decode", "prefill", "mixed", "wide")
 PER_CONFIG_STEPS = 200
 
 
+# --batches N: the workload with N batches drawn from its own distributions (a smaller
+# case of the same kernel for ncu captures that must stay within a few GB); None = as named.
+SUB_BATCHES = None
+
+
 def load_batch(config: str, variant: str, dev):
     import workloads
-    batch = workloads.make_batch(config, dev, variable_extra=2 if variant == "variable" else None)
+    batch = workloads.make_batch(config, dev, B=SUB_BATCHES, variable_extra=2 if variant == "variable" else None)
     if variant == "temperature":
         batch = workloads.with_temperatures(batch, seed=11)
     return batch
@@ -67,7 +72,16 @@ def load_batch(config: str, variant: str, dev):
 
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the row kernel,
 # keyed by workload, valid only while the kernels' device code hashes to the recorded value.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "decode": {"source_hash": "5045b39ad67b0d19", "bytes_per_launch": 131499008,
+               "how": "one-pass launch list (dram__bytes_read.sum + dram__bytes_write.sum), median of 205 launches"},
+    "prefill": {"source_hash": "5045b39ad67b0d19", "bytes_per_launch": 903140352,
+                "how": "--set full capture of one launch (its writes include lines the replay restored)"},
+    "mixed": {"source_hash": "5045b39ad67b0d19", "bytes_per_launch": 3347989612,
+              "how": "one-pass capture of a 12-batch sub-batch (1298 rows), scaled by rows to 5476"},
+    "wide": {"source_hash": "5045b39ad67b0d19", "bytes_per_launch": 22189563751,
+             "how": "one-pass capture of a 3-batch sub-batch (2670 rows), scaled by rows to 21598"},
+}
 
 
 def _code_only(text: str) -> str:
@@ -416,10 +430,13 @@ class Workload:
         alg = self.algorithmic_bytes()
         achieved = alg / (compute_ms / 1e3) / 1e9
         peak, peak_src = measured_peak_hbm()
-        traffic = None
+        traffic, traffic_how = None, "no ncu capture recorded for this workload and kernel code"
         rec = NCU_TRAFFIC.get(self.config if self.variant == "none" else f"{self.config}/{self.variant}")
-        if rec and rec.get("source_hash") == kernel_source_hash():
-            traffic = rec["bytes_per_launch"]
+        if rec and SUB_BATCHES is None:
+            if rec.get("source_hash") == kernel_source_hash():
+                traffic, traffic_how = rec["bytes_per_launch"], rec["how"]
+            else:
+                traffic_how = "the kernels' device code changed since the recorded ncu capture"
         entry = ("lp_ragged_shard_partials" if self.sharded else
                  ("lp_ragged_compute_ex" if self.extended else "lp_ragged_compute"))
         forced = os.environ.get("LP_RAGGED_KERNEL")
@@ -432,6 +449,7 @@ class Workload:
                 "timing": f"CUDA events around one CUDA-graph replay of {self.n_ev} back-to-back compute launches, "
                           f"same stream, right after the timed steps",
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "traffic_source": traffic_how,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": alg,
                 "compute_ms_per_launch": round(compute_ms, 5)}
@@ -448,6 +466,10 @@ def gpu_uuid(dev):
         return u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         return None
+
+
+def sub_batch_text() -> str:
+    return "" if SUB_BATCHES is None else f" [sub-batch for profiling: {SUB_BATCHES} batches, same distributions]"
 
 
 def run_ours(args, rank: int, world: int, dist):
@@ -561,8 +583,8 @@ def run_ours(args, rank: int, world: int, dist):
         "metric": METRIC, "value": whole_job_rows_per_s(R, world, ms_step), "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.config] + VARIANT_TEXT[args.variant], "name": args.config,
-                   "variant": args.variant, "B": B, "T": T, "T_logits": T_logits, "V": V,
+        "config": {"workload": WORKLOAD_TEXT[args.config] + VARIANT_TEXT[args.variant] + sub_batch_text(),
+                   "name": args.config, "variant": args.variant, "B": B, "T": T, "T_logits": T_logits, "V": V,
                    "levels": levels, "rows_per_gpu": R, "parallelism": f"replicas x{world} (independent batches)",
                    "l2": wl.l2_note(),
                    "launch": "the K timed steps (lp_ragged_step: plan + row kernel; vocab8: plan, partials, merge) "
@@ -581,7 +603,7 @@ def run_ours(args, rank: int, world: int, dist):
     # The other workloads in the same run, each timed the same way (device timing; the
     # headline alone carries e2e and the oracle's rate), one at a time so that each one's
     # logits are freed before the next is built.
-    if args.variant == "none" and not args.no_per_config:
+    if args.variant == "none" and not args.no_per_config and SUB_BATCHES is None:
         per = {}
         launches = 0
         for name in PER_CONFIG:
@@ -649,8 +671,9 @@ def run_reference(args, rank: int, world: int):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.config] + VARIANT_TEXT[args.variant], "name": args.config,
-                   "variant": args.variant, "B": batch.B, "T": batch.tokens.numel(), "T_logits": batch.T,
+        "config": {"workload": WORKLOAD_TEXT[args.config] + VARIANT_TEXT[args.variant] + sub_batch_text(),
+                   "name": args.config, "variant": args.variant, "B": batch.B, "T": batch.tokens.numel(),
+                   "T_logits": batch.T,
                    "V": batch.V, "levels": batch.levels},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -671,10 +694,18 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batches", type=int, default=None,
+                    help="profiling aid: the workload with this many batches from its own distributions "
+                         "(labelled in config.workload; not a headline number)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only the headline workload (no per_config entries for the others)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.batches is not None:
+        if args.batches < 1:
+            ap.error("--batches must be >= 1")
+        global SUB_BATCHES
+        SUB_BATCHES = args.batches
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
