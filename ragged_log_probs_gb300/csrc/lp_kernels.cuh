@@ -356,6 +356,29 @@ struct Selector {
         cnt = cnt > 32 ? cnt - 32 : 0;
         thr = fmaxf(thr, L.kth(K));
     }
+    // The last flush of a piece when at most 8 candidates wait and K <= 8, for callers
+    // that read only the list's first 8 entries afterwards: the candidates sorted in
+    // lanes 0..7 (a bitonic sort of 8) and merged with the list's first 8. Entries 8..31
+    // are left unordered. The threshold is not updated.
+    __device__ __forceinline__ void flush_top8(int lane) {
+        __syncwarp();
+        float x = lane < cnt ? cx[lane] : neg_inf();
+        uint32_t id = lane < cnt ? ci[lane] : kPadId;
+#pragma unroll
+        for (int k = 2; k <= 8; k <<= 1) {
+#pragma unroll
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const float ox = __shfl_xor_sync(kFull, x, j);
+                const uint32_t oid = __shfl_xor_sync(kFull, id, j);
+                const bool lower = (lane & j) == 0;
+                const bool desc = (lane & k) == 0;
+                const bool ob = better(ox, oid, x, id);
+                if ((lower == desc) ? ob : !ob) { x = ox; id = oid; }
+            }
+        }
+        if constexpr (SLOTS == 1) merge_top<8>(L.x[0], L.id[0], x, id, lane);
+        cnt = 0;
+    }
     // Append the elements of one ring block flagged in mk: bit 4u+k is element k of the
     // lane's vector u, whose value sits at slot_f[128u + 4 lane + k] and whose id is
     // idb + 128u + k. Warp-uniform call, one ballot round per element a lane appends
@@ -686,7 +709,10 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
         }
     }
     if constexpr (TOPK) {
-        if (sel.cnt > 0) sel.flush(lane);
+        // The row-queue kernel reads only the first K entries after this (its tree merges
+        // 8 wide for K <= 8); the warp-range kernel merges whole lists.
+        if (SLOTS == 1 && TABW > 0 && sel.K <= 8u && sel.cnt > 0 && sel.cnt <= 8) sel.flush_top8(lane);
+        else if (sel.cnt > 0) sel.flush(lane);
     }
     // Leave the reference at the lane's maximum (c = m * k), the form the merges and the
     // row tuples use.
@@ -1190,17 +1216,19 @@ struct __align__(128) CtaMerge {
 };
 
 // Next-token logits (one logits row per batch: output row o reads logits row o). Warp w
-// of a CTA that starts on a task of its own (blockIdx.x < min(B * S, SMs)) prefetches
-// the first kPrefetchVec vectors of its part of that task into L2, before the offsets are
-// read, so that HBM already works during that round trip. The range is computed as in
-// stream_piece and lies inside logits row o (o < B = rows of logits); the prefetch is a
-// hint and changes no result, even when the offsets turn out to be bad.
-constexpr uint32_t kPrefetchVec = 512;  // 8 KB per warp
+// of CTA i < B * S prefetches into L2 the first kPrefetchVec vectors of its part of task
+// i, before the dependency wait or the offsets: HBM already works meanwhile. Task i is
+// the CTA's own for i < min(B * S, SMs), and for a later CTA the task the queue hands
+// out i-th; whichever CTA takes a task, every task is streamed, so no prefetched line
+// goes unread. The range is computed as in stream_piece and lies inside logits row
+// o (o < B = rows of logits); the prefetch is a hint and changes no result, even when
+// the offsets turn out to be bad.
+constexpr uint32_t kPrefetchVec = 1024;  // 16 KB per warp
 
 template <int NW>
 __device__ __forceinline__ void prefetch_own_task(const RowsParams& p, int w) {
-    const uint32_t S = p.split, ntask = p.B * S, nA = ntask < p.num_sms ? ntask : p.num_sms;
-    if (blockIdx.x >= nA) return;
+    const uint32_t S = p.split, ntask = p.B * S;
+    if (blockIdx.x >= ntask) return;
     const uint32_t o = blockIdx.x / S, piece = blockIdx.x - o * S;
     const uint32_t pq0 = (uint32_t)(((uint64_t)p.nq * piece) / S);
     const uint32_t pq1 = (uint32_t)(((uint64_t)p.nq * (piece + 1)) / S);
