@@ -141,6 +141,10 @@ struct RowsParams {
     // position its own logits row): valid offsets are then 0..B, so output row o is batch
     // o and reads logits row o, and a CTA streams its first task before any offset is read.
     uint32_t next_token;
+    // Row-queue kernel, a step on next-token logits with more tasks than SMs but no more
+    // than CTAs: every task has a CTA from the start (see k_rows_cta), so no CTA waits for
+    // the plan (which clears the queue) before its first task.
+    uint32_t spread_first;
 };
 
 // Row tuple of one vocab shard (lp_ragged_shard_partials), u32 words:
@@ -1246,7 +1250,7 @@ constexpr int kQueueWarps = LP_QUEUE_WARPS;
 constexpr int kQueueStages = LP_QUEUE_STAGES;
 constexpr int kQueueUnroll = LP_QUEUE_UNROLL;
 
-template <int SLOTS, bool TOPK, int U, int STAGES, int NW, bool EXT>
+template <int SLOTS, bool TOPK, int U, int STAGES, int NW, bool EXT, bool STEP>
 __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     extern __shared__ __align__(128) unsigned char s_raw[];
     trigger_dependents();
@@ -1264,7 +1268,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
     const uint32_t* out_off = p.out_off;
     const uint8_t* echo = p.echo;
     const bool fast = LP_NEXT_TOKEN_FAST && p.next_token != 0u;
-    const bool early = p.early && (fast || p.stage_offsets);
+    const bool early = STEP && p.early && (fast || p.stage_offsets);  // STEP: lp_ragged_step's launch
     uint32_t status, R;
     if (fast && early) {
         // A step on next-token logits: the plan, which let this launch start only once all
@@ -1325,7 +1329,13 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
                           (S > 1 && R > p.split_rows) || (p.out_rows && R > p.out_rows);
     const bool bad = (status & kStatusOffsets) || too_many;
     const uint32_t ntask = bad ? 0u : R * S;
-    const uint32_t nA = ntask < p.num_sms ? ntask : p.num_sms;
+    // In a step on next-token logits (spread_first) the CTAs after the first SMs take the
+    // remaining tasks by a fixed map instead of the queue, which the plan clears: CTA
+    // SMs + j takes task SMs + k for the j = floor(k * (CTAs - SMs) / (tasks - SMs)), so
+    // the second tasks spread evenly over the CTAs in dispatch order (and thus over the
+    // SMs); every CTA then holds at most one task and nA = tasks.
+    const bool spread = STEP && p.spread_first != 0u && ntask > p.num_sms && ntask <= gridDim.x;
+    const uint32_t nA = spread ? ntask : (ntask < p.num_sms ? ntask : p.num_sms);
     // Task -> row o, piece of the row, pieces of the row, partial slot of its piece 0.
     struct TaskRef {
         uint32_t o, piece, n, slot0;
@@ -1335,7 +1345,7 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         return TaskRef{oo, task - oo * S, S, oo * S};
     };
     // A CTA without a task of its own goes to the queue (counters): after the plan.
-    if (early && blockIdx.x >= nA) pdl_wait();
+    if (early && !spread && blockIdx.x >= nA) pdl_wait();
     // Every CTA asks the queue after each task (and a CTA without a task of its own once at
     // its start) until it is told there is none: one request per queued task, one refusal
     // per CTA that asks. Every CTA sees the same task count, so the number of requests is
@@ -1353,8 +1363,20 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         cm.thr = 0u;
         cm.fast_ok = 2u;
         uint32_t task = ntask;
-        if (blockIdx.x < nA) task = blockIdx.x;
-        else if (ntask > nA) task = next_task();
+        if (spread) {
+            const uint32_t f = p.num_sms, g2 = gridDim.x - f, rest = ntask - f;
+            if (blockIdx.x < f) {
+                task = blockIdx.x;
+            } else {
+                const uint32_t j = blockIdx.x - f;
+                const uint32_t k = (uint32_t)(((uint64_t)j * rest + g2 - 1u) / g2);
+                if (k < rest && (uint32_t)(((uint64_t)k * g2) / rest) == j) task = f + k;
+            }
+        } else if (blockIdx.x < nA) {
+            task = blockIdx.x;
+        } else if (ntask > nA) {
+            task = next_task();
+        }
         cm.row = task;
         if (blockIdx.x == 0 && too_many && !(status & kStatusOffsets)) atomicOr(p.status, kStatusOffsets);
     }

@@ -39,10 +39,12 @@ constexpr size_t kQueueDynSmemBudget = 208 * 1024;
 #ifndef LP_PDL
 #define LP_PDL 1  // launch the row kernel as a programmatic dependent of the plan
 #endif
-// (levels 0 | 1..5 | 6) x (warp ranges | row queue) x (plain | extended inputs)
-constexpr int kKinds = 2;
+// (levels 0 | 1..5 | 6) x (warp ranges | row queue | row queue in a one-call step)
+// x (plain | extended inputs). The step's row-queue instantiation holds the code that
+// streams before the plan has finished; the others compile without it.
+constexpr int kKinds = 3;
 constexpr int kVariants = 3 * kKinds * 2;
-enum Kind { kWarpRanges = 0, kRowQueue = 1 };
+enum Kind { kWarpRanges = 0, kRowQueue = 1, kRowQueueStep = 2 };
 
 struct DeviceInfo {
     bool ready = false;
@@ -63,9 +65,12 @@ RowsKernel variant_kernel(int v) {
         case 0: return &lpk::k_rows<1, false, kUnroll, kStages, EXT>;
         case 1: return &lpk::k_rows<1, true, kUnroll, kStages, EXT>;
         case 2: return &lpk::k_rows<2, true, kUnroll, kStages, EXT>;
-        case 3: return &lpk::k_rows_cta<1, false, kQU, kQS, kQW, EXT>;
-        case 4: return &lpk::k_rows_cta<1, true, kQU, kQS, kQW, EXT>;
-        default: return &lpk::k_rows_cta<2, true, kQU, kQS, kQW, EXT>;
+        case 3: return &lpk::k_rows_cta<1, false, kQU, kQS, kQW, EXT, false>;
+        case 4: return &lpk::k_rows_cta<1, true, kQU, kQS, kQW, EXT, false>;
+        case 5: return &lpk::k_rows_cta<2, true, kQU, kQS, kQW, EXT, false>;
+        case 6: return &lpk::k_rows_cta<1, false, kQU, kQS, kQW, EXT, true>;
+        case 7: return &lpk::k_rows_cta<1, true, kQU, kQS, kQW, EXT, true>;
+        default: return &lpk::k_rows_cta<2, true, kQU, kQS, kQW, EXT, true>;
     }
 }
 
@@ -75,7 +80,8 @@ RowsKernel variant_kernel(int v) {
     return v >= kPerExt ? variant_kernel<true>(v - kPerExt) : variant_kernel<false>(v);
 }
 Kind kind_of(int v) { return (Kind)((v % kPerExt) / 3); }
-int block_threads(int v) { return kind_of(v) == kRowQueue ? kQW * 32 : lpk::kThreads; }
+bool is_queue(int v) { return kind_of(v) != kWarpRanges; }
+int block_threads(int v) { return is_queue(v) ? kQW * 32 : lpk::kThreads; }
 const void* variant_fn(int v) { return reinterpret_cast<const void*>(variant_kernel(v)); }
 
 int variant_of(uint32_t levels) { return levels == 0 ? 0 : (levels < 6 ? 1 : 2); }
@@ -100,7 +106,7 @@ bool device_info(int* dev_out, DeviceInfo** info) {
 // Allow the variant's largest dynamic shared memory (once per device); false on failure.
 bool set_smem_attr(DeviceInfo* d, int v) {
     if (d->smem_attr[v]) return true;
-    const size_t dyn = kind_of(v) == kRowQueue ? kMaxDynSmemQueue : kMaxDynSmem;
+    const size_t dyn = is_queue(v) ? kMaxDynSmemQueue : kMaxDynSmem;
     if (cudaFuncSetAttribute(variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
@@ -289,6 +295,7 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     p.out_rows = out_rows;
     // next-token logits: one logits row per batch and per position
     p.next_token = (T == B && T_logits == B && input_row_offsets == nullptr) ? 1u : 0u;
+    p.spread_first = 0;
 
     const uint32_t staged_arrays = (p.loff != p.off) ? 3u : 2u;
     const size_t smem =
@@ -311,7 +318,7 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     size_t launch_smem = smem;
     unsigned block = lpk::kThreads;
     if (queue) {
-        v += 3 * kRowQueue;
+        v += 3 * (early ? kRowQueueStep : kRowQueue);
         block = kQW * 32;
         launch_smem = smem - kRingBytes + kQueueRingBytes;
         if (launch_smem > kQueueDynSmemBudget) {  // very many batches: read offsets from global memory
@@ -334,6 +341,8 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
         if (S < 1) S = 1;
         if (S > kMaxSplit) S = kMaxSplit;
         p.split = S;
+        // a step on next-token logits whose tasks fit the CTAs: no CTA waits for the plan
+        p.spread_first = (early && p.next_token && (uint64_t)B * S <= grid) ? 1u : 0u;
         // rows the workspace holds a ticket (after the 2 queue words) and S piece slots for
         const uint32_t by_words = g_max - 2u;
         const uint32_t by_slots = 2u * g_max / S;
