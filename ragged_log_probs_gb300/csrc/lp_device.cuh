@@ -220,6 +220,21 @@ __device__ __forceinline__ void merge_top(float& ax, uint32_t& ai, float bx, uin
     }
 }
 
+// merge_top<N> with b already reversed: lane l holds b[(N-1) - (l mod N)] (loaded that
+// way from shared memory, or sorted ascending), which saves merge_top's first shuffle.
+template <int N>
+__device__ __forceinline__ void merge_top_rev(float& ax, uint32_t& ai, float rx, uint32_t ri, int lane) {
+    static_assert(N == 8 || N == 16 || N == 32, "group of 8, 16 or 32 lanes");
+    if (better(rx, ri, ax, ai)) { ax = rx; ai = ri; }
+#pragma unroll
+    for (int j = N / 2; j > 0; j >>= 1) {
+        const float ox = __shfl_xor_sync(kFull, ax, j);
+        const uint32_t oid = __shfl_xor_sync(kFull, ai, j);
+        const bool lower = (lane & j) == 0;
+        if (better(ox, oid, ax, ai) == lower) { ax = ox; ai = oid; }
+    }
+}
+
 // Packed fp32 pair arithmetic (one instruction for two lanes of data, sm_100+).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     float2 d;

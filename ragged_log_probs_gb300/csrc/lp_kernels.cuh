@@ -361,9 +361,10 @@ struct Selector {
         thr = fmaxf(thr, L.kth(K));
     }
     // The last flush of a piece when at most 8 candidates wait and K <= 8, for callers
-    // that read only the list's first 8 entries afterwards: the candidates sorted in
-    // lanes 0..7 (a bitonic sort of 8) and merged with the list's first 8. Entries 8..31
-    // are left unordered. The threshold is not updated.
+    // that read only the list's first 8 entries afterwards: the candidates sorted
+    // ascending in lanes 0..7 (a bitonic sort of 8), which pairs them reversed with the
+    // list's first 8 for the merge. Entries 8..31 are left unordered. The threshold is
+    // not updated.
     __device__ __forceinline__ void flush_top8(int lane) {
         __syncwarp();
         float x = lane < cnt ? cx[lane] : neg_inf();
@@ -375,12 +376,12 @@ struct Selector {
                 const float ox = __shfl_xor_sync(kFull, x, j);
                 const uint32_t oid = __shfl_xor_sync(kFull, id, j);
                 const bool lower = (lane & j) == 0;
-                const bool desc = (lane & k) == 0;
+                const bool asc = (lane & k) == 0;
                 const bool ob = better(ox, oid, x, id);
-                if ((lower == desc) ? ob : !ob) { x = ox; id = oid; }
+                if ((lower == asc) ? !ob : ob) { x = ox; id = oid; }
             }
         }
-        if constexpr (SLOTS == 1) merge_top<8>(L.x[0], L.id[0], x, id, lane);
+        if constexpr (SLOTS == 1) merge_top_rev<8>(L.x[0], L.id[0], x, id, lane);
         cnt = 0;
     }
     // Append the elements of one ring block flagged in mk: bit 4u+k is element k of the
@@ -1400,18 +1401,23 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
 #pragma unroll
             for (int st = 1; st < NW; st <<= 1) {
                 if ((w & (2 * st - 1)) == 0 && w + st < NW) {
-                    float bx[SLOTS];
-                    uint32_t bi[SLOTS];
-#pragma unroll
-                    for (int k = 0; k < SLOTS; ++k) {
-                        bx[k] = cm.list_x[w + st][lane + 32 * k];
-                        bi[k] = cm.list_i[w + st][lane + 32 * k];
-                    }
                     if constexpr (SLOTS == 1) {
-                        if (tree_width == 8) merge_top<8>(L.x[0], L.id[0], bx[0], bi[0], lane);
-                        else if (tree_width == 16) merge_top<16>(L.x[0], L.id[0], bx[0], bi[0], lane);
-                        else merge_top<32>(L.x[0], L.id[0], bx[0], bi[0], lane);
+                        // the partner's list read reversed within each group of tree_width
+                        const int g = tree_width - 1;
+                        const int src = (lane & ~g) | (g - (lane & g));
+                        const float rx = cm.list_x[w + st][src];
+                        const uint32_t ri = cm.list_i[w + st][src];
+                        if (tree_width == 8) merge_top_rev<8>(L.x[0], L.id[0], rx, ri, lane);
+                        else if (tree_width == 16) merge_top_rev<16>(L.x[0], L.id[0], rx, ri, lane);
+                        else merge_top_rev<32>(L.x[0], L.id[0], rx, ri, lane);
                     } else {
+                        float bx[SLOTS];
+                        uint32_t bi[SLOTS];
+#pragma unroll
+                        for (int k = 0; k < SLOTS; ++k) {
+                            bx[k] = cm.list_x[w + st][lane + 32 * k];
+                            bi[k] = cm.list_i[w + st][lane + 32 * k];
+                        }
                         merge_lists<SLOTS>(L.x, L.id, bx, bi, lane);
                     }
 #pragma unroll
