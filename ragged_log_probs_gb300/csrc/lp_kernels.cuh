@@ -1221,8 +1221,8 @@ struct __align__(128) CtaMerge {
 };
 
 // Next-token logits (one logits row per batch: output row o reads logits row o). Warp w
-// of CTA i < B * S prefetches into L2 the first kPrefetchVec vectors of its part of task
-// i, before the dependency wait or the offsets: HBM already works meanwhile. Task i is
+// of CTA i < B * S prefetches into L2 the first vectors of its part of task i (8 or
+// 16 KB), before the dependency wait or the offsets: HBM already works meanwhile. Task i is
 // the CTA's own for i < min(B * S, SMs), and for a later CTA the task the queue hands
 // out i-th; whichever CTA takes a task, every task is streamed, so no prefetched line
 // goes unread. The range is computed as in stream_piece and lies inside logits row
@@ -1243,7 +1243,10 @@ __device__ __forceinline__ void prefetch_own_task(const RowsParams& p, int w) {
     const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
     const uint32_t qf = a ? 1u : 0u, qe = (p.V + (uint32_t)a) >> 2;
     const uint32_t qa = max(q0, qf), qb = max(min(q1, qe), qa);
-    const uint32_t n = min(qb - qa, kPrefetchVec);
+    // 16 KB per warp for a CTA's own first task when the launch has at most two tasks per
+    // SM and a small top-k (cheap blocks: the prefetch is consumed soon), else 8 KB
+    const bool big = blockIdx.x < p.num_sms && p.K <= 7u && ntask <= 2u * p.num_sms;
+    const uint32_t n = min(qb - qa, big ? kPrefetchVec : kPrefetchVec / 2u);
     if (n) prefetch_l2_bulk(rowp - a + 4 * (size_t)qa, 16u * n);
 }
 
