@@ -616,7 +616,7 @@ __device__ __forceinline__ void select_block(const float4 (&v)[U], float bm, uin
 // of those 32 values is an element of a different (warp, lane) stream of the row, so K
 // of them are K distinct elements, and with TABW times more elements behind each value
 // the bound sits much closer to the row's true K-th best than one warp's own.
-template <int SLOTS, bool TOPK, int U, int STAGES, int TABW = 0>
+template <int SLOTS, bool TOPK, int U, int STAGES, int TABW = 0, int IL = 1>
 __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint32_t q0, uint32_t q1, int lane,
                                              LaneSum& ls, Selector<SLOTS>& sel, bool& t_here, uint32_t t,
                                              float& xt, float4* ring, uint32_t* shared_thr = nullptr,
@@ -630,8 +630,14 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     // after them at most the row's partial first and last vectors (unaligned rows only).
     const uint32_t qa = max(q0, qf);
     const uint32_t qb = max(min(q1, qe), qa);
-    const uint32_t nblk = (qb - qa + 32u * U - 1u) / (32u * U);
-    const uint32_t rem = (qb - qa) % (32u * U);  // vectors in the last block when it is partial
+    // IL > 1: the IL warps of a CTA share the piece block by block, warp w taking blocks
+    // w, w + IL, w + 2 IL, ... (each warp's bytes spread over the whole piece, so the warps
+    // meet the same HBM and the same share of large values); IL = 1: the warp streams all.
+    const uint32_t wi = IL > 1 ? (uint32_t)w : 0u;
+    const uint32_t nb_all = (qb - qa + 32u * U - 1u) / (32u * U);
+    const uint32_t nblk = nb_all > wi ? (nb_all - wi + IL - 1u) / IL : 0u;
+    // vectors in the warp's last block when it is the piece's partial last block
+    const uint32_t rem = (nb_all != 0u && (nb_all - 1u) % IL == wi) ? (qb - qa) % (32u * U) : 0u;
 
     // ---- bulk: U vectors per lane per block ---------------------------------------------
     // The issue side walks the source and the ring slots by running offsets (no index
@@ -640,7 +646,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     // ring slots with -inf (no term, no maximum; the top-k keeps ids below id_end), so
     // the piece's tail streams through the ring like the rest.
     constexpr uint32_t kStage = U * 512u;  // ring bytes per block and warp
-    const float* src = vbase + 4 * (size_t)(qa + lane);
+    const float* src = vbase + 4 * ((size_t)qa + 32u * U * wi + lane);
     const uint32_t ring_lane = (uint32_t)__cvta_generic_to_shared(ring + lane);
     uint32_t put = 0, get = 0;  // ring offsets of the next block to issue / to reduce
     uint32_t unissued = nblk;
@@ -648,7 +654,7 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
         if (unissued) {
             if (unissued == 1u && rem != 0u) cp_async16_run_pad<U>(ring_lane + put, src, (int)rem - lane);
             else cp_async16_run<U>(ring_lane + put, src);
-            src += 128 * U;
+            src += 128 * U * IL;
             put = put == (STAGES - 1) * kStage ? 0u : put + kStage;
             --unissued;
         }
@@ -662,8 +668,12 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
     // after the first copies are in flight, so the wait for the token id overlaps them.
     const int64_t e_lo = 4 * (int64_t)q0 - a, e_hi = 4 * (int64_t)q1 - a;
     t_here = t < V && (int64_t)t >= e_lo && (int64_t)t < e_hi;
+    if (IL > 1 && t_here) {  // the warp of the target's block; warp 0 for the row's edges
+        const uint32_t qt = (t + (uint32_t)a) >> 2;
+        t_here = (qt >= qa && qt < qb) ? ((qt - qa) / (32u * U)) % IL == wi : wi == 0u;
+    }
     bool xt_pending = t_here;
-    uint32_t idb = 4u * (qa + (uint32_t)lane) - (uint32_t)a;
+    uint32_t idb = 4u * (qa + 32u * U * wi + (uint32_t)lane) - (uint32_t)a;
     const uint32_t id_end = 4u * qb - (uint32_t)a;  // ids of the ring's padding start here
     for (uint32_t blk = 0; blk < nblk; ++blk) {
         issue();
@@ -689,14 +699,14 @@ __device__ __forceinline__ void stream_piece(const float* rowp, uint32_t V, uint
 
         select_block<SLOTS, TOPK, U, TABW>(v, bm, blk, blk + 1u == nblk && rem != 0u, idb, id_end, slot_f, ls, sel,
                                            lane, shared_thr, lane_tab, w);
-        idb += 128u * U;
+        idb += 128u * U * IL;
     }
     if (xt_pending && lane == 0) xt = rowp[t];
 
     // ---- edges: the row's partial first and last vectors (rows that do not start or end
-    // on a 16-byte boundary), one checked vector per lane
+    // on a 16-byte boundary), one checked vector per lane; warp 0 of an interleaved piece
 #pragma unroll 1
-    for (int part = 0; part < 2; ++part) {
+    for (int part = 0; part < (wi == 0u ? 2 : 0); ++part) {
         const uint32_t lo = part ? qb : q0;
         const uint32_t hi = part ? q1 : min(qa, q1);
         for (uint32_t qs = lo; qs < hi; qs += 32) {
@@ -1237,17 +1247,18 @@ __device__ __forceinline__ void prefetch_own_task(const RowsParams& p, int w) {
     const uint32_t o = blockIdx.x / S, piece = blockIdx.x - o * S;
     const uint32_t pq0 = (uint32_t)(((uint64_t)p.nq * piece) / S);
     const uint32_t pq1 = (uint32_t)(((uint64_t)p.nq * (piece + 1)) / S);
-    const uint32_t q0 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * w) / NW);
-    const uint32_t q1 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * (w + 1)) / NW);
     const float* rowp = p.logits + (size_t)o * p.V;
     const int a = (int)(((uintptr_t)rowp >> 2) & 3u);
     const uint32_t qf = a ? 1u : 0u, qe = (p.V + (uint32_t)a) >> 2;
-    const uint32_t qa = max(q0, qf), qb = max(min(q1, qe), qa);
+    const uint32_t qa = max(pq0, qf), qb = max(min(pq1, qe), qa);
     // 16 KB per warp for a CTA's own first task when the launch has at most two tasks per
-    // SM and a small top-k (cheap blocks: the prefetch is consumed soon), else 8 KB
+    // SM and a small top-k (cheap blocks: the prefetch is consumed soon), else 8 KB. The
+    // warps take the piece block by block, so together they start on its first NW * n
+    // vectors: warp w prefetches the w-th n of them.
     const bool big = blockIdx.x < p.num_sms && p.K <= 7u && ntask <= 2u * p.num_sms;
-    const uint32_t n = min(qb - qa, big ? kPrefetchVec : kPrefetchVec / 2u);
-    if (n) prefetch_l2_bulk(rowp - a + 4 * (size_t)qa, 16u * n);
+    const uint32_t n = big ? kPrefetchVec : kPrefetchVec / 2u;
+    const uint32_t c0 = min(qa + (uint32_t)w * n, qb), c1 = min(c0 + n, qb);
+    if (c1 > c0) prefetch_l2_bulk(rowp - a + 4 * (size_t)c0, 16u * (c1 - c0));
 }
 
 constexpr int kQueueWarps = LP_QUEUE_WARPS;
@@ -1479,10 +1490,8 @@ __global__ void __launch_bounds__(NW * 32, 24 / NW) k_rows_cta(RowsParams p) {
         Selector<SLOTS> sel;
         sel.init(s_cx[w], s_ci[w], K);
         float xt = 0.f;
-        const uint32_t wq0 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * w) / NW);
-        const uint32_t wq1 = pq0 + (uint32_t)(((uint64_t)(pq1 - pq0) * (w + 1)) / NW);
-        stream_piece<SLOTS, TOPK, U, STAGES, NW>(rowp, V, wq0, wq1, lane, ls, sel, t_here, t_loc, xt, ring, &cm.thr,
-                                                 &cm.lane_max[0][0], w);
+        stream_piece<SLOTS, TOPK, U, STAGES, NW, NW>(rowp, V, pq0, pq1, lane, ls, sel, t_here, t_loc, xt, ring,
+                                                     &cm.thr, &cm.lane_max[0][0], w);
         if (early) pdl_wait();  // the plan has finished before the queue, tickets or status are touched
         if (fast && early && threadIdx.x == 0) {
             // the plan's outputs this task's checks need, read during the merges below

@@ -135,13 +135,18 @@ def test_step_next_token_prefetch(B, V, monkeypatch):
     check_equal(workloads.make_next_token_batch(B, V, levels=3, device="cuda", seed=B), f"next-token {B}x{V}")
 
 
-def test_step_next_token_bad_offsets_write_no_row():
-    # One logits row per batch, so the prefetch guesses row o for output row o; with
-    # non-monotone offsets the guess is wrong, nothing is written and the status says so.
+@pytest.mark.parametrize("B", [5, 200])
+def test_step_next_token_bad_offsets_write_no_row(B, monkeypatch):
+    # One logits row per batch, so the row kernel streams row o for output row o before it
+    # has seen any offset; with non-monotone offsets that guess is wrong, nothing is written
+    # and the status says so (200 rows: more tasks than SMs, the second ones by a fixed map).
+    monkeypatch.setenv("LP_RAGGED_KERNEL", "queue")
     g = torch.Generator().manual_seed(17)
-    x = torch.randn(5, 70001, generator=g).cuda()
-    b = workloads.make_custom_batch(x, [1] * 5, [0] * 5, 3, seed=17)
-    b.logit_row_offsets.copy_(torch.tensor([0, 1, 3, 2, 4, 5], dtype=torch.int32))
+    x = torch.randn(B, 70001, generator=g).cuda()
+    b = workloads.make_custom_batch(x, [1] * B, [0] * B, 3, seed=17)
+    off = list(range(B + 1))
+    off[2], off[3] = 3, 2
+    b.logit_row_offsets.copy_(torch.tensor(off, dtype=torch.int32))
     R, status, _, g_lp, g_tok = run_step(b, sentinel=True)
     assert status & BIT_OFFSETS
     assert np.all(g_lp == 123.25) and np.all(g_tok == 77)
