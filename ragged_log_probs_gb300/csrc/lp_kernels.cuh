@@ -494,7 +494,7 @@ __device__ __forceinline__ void select_block(const float4 (&v)[U], float bm, uin
         // elements already seen, so no element below it can be in the top-k: a
         // threshold that follows the warp's true K-th best at the cost of one float
         // sort, refreshed on blocks 0, 1, 2 and 4 (it rises fastest early) and then
-        // every kThrEvery blocks.
+        // every kThrEvery blocks (row queue at K <= 7: see refresh_due_q).
         if ((TABW > 0 && sel.K <= 7u) ? refresh_due_q(blk, w) : refresh_due(blk)) {
             float lm = ls.m;
             uint32_t kk = sel.K;
@@ -1201,18 +1201,19 @@ __global__ void __launch_bounds__(kThreads, LP_MIN_BLOCKS) k_rows(RowsParams p) 
 }
 
 // ---------------------------------------------------------------------------------
-// Few rows (up to three per SM; e.g. next-token logits for a decode batch): CTAs of NW warps take tasks; a task is a whole row, or, when
-// there are fewer rows than twice the SMs, one of S contiguous pieces of a row
-// (split-vocab, chosen on the host: S = min(2*SMs / rows, row length / 42 KB, 64) for rows
-// of 192 KB or more). The
-// CTA's warps split the task into NW contiguous parts and merge their results in shared
-// memory; a whole row is written at once, a piece is published to the workspace and the
-// CTA that takes the row's last ticket merges the S pieces with all its warps (each warp
-// merges every NW-th piece, then the shared-memory tree). The first CTA on each SM starts
-// on a task of its own without an atomic, every later task comes from one queue counter,
+// Few rows (up to three per SM; e.g. next-token logits for a decode batch): CTAs of NW
+// warps take tasks; a task is a whole row, or, when there are fewer rows than twice the
+// SMs, one of S contiguous pieces of a row (split-vocab, chosen on the host: S = min(2*SMs
+// / rows, row length / 42 KB, 64) for rows of 192 KB or more). The CTA's warps take the
+// task's 2 KB blocks in turn (warp w: blocks w, w + NW, ...) and merge their results in
+// shared memory; a whole row is written at once, a piece is published to the workspace
+// and the CTA that takes the row's last ticket merges the S pieces with all its warps
+// (each warp merges every NW-th piece, then the shared-memory tree). The first CTA on each
+// SM starts on a task of its own without an atomic, every later task comes from one queue
+// counter (in a next-token step with at most one task per CTA, from a fixed map instead),
 // so all SMs stream from the start. The warps of a CTA share their lanes' running maxima
-// for the top-k threshold (see stream_piece). The last CTA to leave resets the queue
-// words for the next call; the merging CTA resets its row's ticket.
+// for the top-k threshold (see stream_piece). The request that comes last resets the
+// queue for the next call; the merging CTA resets its row's ticket.
 template <int NW>
 struct __align__(128) CtaMerge {
     float list_x[NW][64];
