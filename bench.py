@@ -73,14 +73,14 @@ def load_batch(config: str, variant: str, dev):
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the row kernel,
 # keyed by workload, valid only while the kernels' device code hashes to the recorded value.
 NCU_TRAFFIC = {
-    "decode": {"source_hash": "f6565778a8e18f72", "bytes_per_launch": 131522304,
+    "decode": {"source_hash": "f6565778a8e18f72", "kernel": "queue", "bytes_per_launch": 131522304,
                "how": "one-pass launch list (dram__bytes_read.sum + dram__bytes_write.sum), median of the 100 "
                       "lp_ragged_compute launches"},
-    "prefill": {"source_hash": "f6565778a8e18f72", "bytes_per_launch": 903528448,
+    "prefill": {"source_hash": "f6565778a8e18f72", "kernel": "warp", "bytes_per_launch": 903528448,
                 "how": "--set full capture of one launch (its writes include lines the replay restored)"},
-    "mixed": {"source_hash": "f6565778a8e18f72", "bytes_per_launch": 3348141893,
+    "mixed": {"source_hash": "f6565778a8e18f72", "kernel": "warp", "bytes_per_launch": 3348141893,
               "how": "one-pass capture of a 12-batch sub-batch (1298 rows), scaled by rows to 5476"},
-    "wide": {"source_hash": "f6565778a8e18f72", "bytes_per_launch": 22188876239,
+    "wide": {"source_hash": "f6565778a8e18f72", "kernel": "warp", "bytes_per_launch": 22188876239,
              "how": "one-pass capture of a 3-batch sub-batch (2670 rows), scaled by rows to 21598"},
 }
 
@@ -119,14 +119,6 @@ def kernel_source_hash() -> str:
             h.update(os.path.basename(f).encode())
             h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
-
-
-def few_rows(rows_bound: int) -> bool:
-    """The library's kernel choice: the row-queue kernel when at most three rows per SM
-    can come out; else the warp-range kernel."""
-    import torch
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return rows_bound <= 3 * sms
 
 
 def algorithmic_bytes(R: int, V: int, W: int, B: int) -> int:
@@ -431,20 +423,18 @@ class Workload:
         alg = self.algorithmic_bytes()
         achieved = alg / (compute_ms / 1e3) / 1e9
         peak, peak_src = measured_peak_hbm()
+        kind = self.lp.row_kernel(self.T_logits, self.T, self.V, self.levels)  # the library's own choice
         traffic, traffic_how = None, "no ncu capture recorded for this workload and kernel code"
         rec = NCU_TRAFFIC.get(self.config if self.variant == "none" else f"{self.config}/{self.variant}")
         if rec and SUB_BATCHES is None:
-            if rec.get("source_hash") == kernel_source_hash():
-                traffic, traffic_how = rec["bytes_per_launch"], rec["how"]
-            else:
+            if rec.get("source_hash") != kernel_source_hash():
                 traffic_how = "the kernels' device code changed since the recorded ncu capture"
+            elif rec.get("kernel") != kind:
+                traffic_how = f"the recorded ncu capture is of the other row kernel ({rec.get('kernel')})"
+            else:
+                traffic, traffic_how = rec["bytes_per_launch"], rec["how"]
         entry = ("lp_ragged_shard_partials" if self.sharded else
                  ("lp_ragged_compute_ex" if self.extended else "lp_ragged_compute"))
-        forced = os.environ.get("LP_RAGGED_KERNEL")
-        if forced in ("warp", "queue"):
-            kind = forced
-        else:
-            kind = "queue" if few_rows(min(self.T, self.T_logits)) else "warp"
         kernel_name = {"warp": f"k_rows ({entry}, warp ranges)", "queue": f"k_rows_cta ({entry}, row queue)"}[kind]
         return {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                 "timing": f"CUDA events around one CUDA-graph replay of {self.n_ev} back-to-back compute launches, "

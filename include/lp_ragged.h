@@ -294,6 +294,15 @@ lp_status lp_ragged_compute_noalloc(const float *logits, uint32_t T, uint32_t V,
 /* Enqueue a copy of the workspace status word (bit c <=> lp_status c) to host. */
 lp_status lp_ragged_read_status(const void *workspace, uint32_t *host_status, lp_stream_t stream);
 
+/*
+ * Which row kernel lp_ragged_compute / lp_ragged_compute_ex / lp_ragged_step launch for
+ * this shape on the current device (diagnostics; no counterpart on the pages): *kind = 1
+ * for the row queue (CTAs of 12 warps take whole rows or row pieces), 0 for warp-owned
+ * ranges of the row space. T_logits, T, V, levels as in lp_ragged_compute_ex. The two
+ * kernels give the same rows. Errors: LP_ERR_NULL, LP_ERR_LEVELS, LP_ERR_CUDA (no device).
+ */
+lp_status lp_ragged_row_kernel(uint32_t T_logits, uint32_t T, uint32_t V, uint32_t levels, int *kind);
+
 /* Static, NUL-terminated description of a status code. */
 const char *lp_ragged_strerror(lp_status status);
 

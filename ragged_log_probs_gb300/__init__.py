@@ -21,7 +21,7 @@ from . import _build
 from .results import LogProbabilities, assemble  # noqa: F401  (host-side result assembly)
 
 __all__ = [
-    "LpError", "lib_path", "load", "workspace_size", "new_workspace", "plan", "compute",
+    "LpError", "lib_path", "load", "workspace_size", "new_workspace", "plan", "compute", "row_kernel",
     "compute_ex", "step", "read_status", "ragged_log_probs", "tuple_bytes", "shard_partials", "shard_merge",
     "gather_shard_tuples", "ragged_log_probs_vocab_parallel", "out_per_token", "STATUS_NAMES", "LogProbabilities", "assemble",
 ]
@@ -80,6 +80,8 @@ def load() -> ctypes.CDLL:
     lib.lp_ragged_shard_merge.restype = ctypes.c_int
     lib.lp_ragged_read_status.argtypes = [vp, vp, vp]
     lib.lp_ragged_read_status.restype = ctypes.c_int
+    lib.lp_ragged_row_kernel.argtypes = [u32, u32, u32, u32, vp]
+    lib.lp_ragged_row_kernel.restype = ctypes.c_int
     lib.lp_ragged_strerror.argtypes = [ctypes.c_int]
     lib.lp_ragged_strerror.restype = ctypes.c_char_p
     _LIB = lib
@@ -411,6 +413,16 @@ def ragged_log_probs_vocab_parallel(logits_shard: torch.Tensor, vocab_base: int,
         if status:
             raise LpError(_first_bit(status), "vocab-parallel ragged log-probabilities (device)")
     return out_off, out_lp, out_tok
+
+
+def row_kernel(T_logits: int, T: int, V: int, levels: int) -> str:
+    """The row kernel the library launches for this shape on the current device:
+    ``"queue"`` (row queue) or ``"warp"`` (warp-owned ranges)."""
+    kind = ctypes.c_int(-1)
+    rc = load().lp_ragged_row_kernel(T_logits, T, V, levels, ctypes.addressof(kind))
+    if rc:
+        raise LpError(rc, "lp_ragged_row_kernel")
+    return "queue" if kind.value == 1 else "warp"
 
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:

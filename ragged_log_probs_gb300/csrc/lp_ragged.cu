@@ -86,6 +86,28 @@ const void* variant_fn(int v) { return reinterpret_cast<const void*>(variant_ker
 
 int variant_of(uint32_t levels) { return levels == 0 ? 0 : (levels < 6 ? 1 : 2); }
 
+// The row kernel for at most r_max scored rows of V logits (R <= min(T, T_logits) is all
+// the host knows before the plan has run). The row queue pays a fixed cost per task (its
+// ring restarts, the CTA's merges), the warp ranges stream on across rows but bound the
+// top-k by one warp's values only; measured on next-token shapes and the workloads:
+// - up to three rows per SM: the row queue (every row starts at once);
+// - rows of 60 KB or more, up to seven per SM: the row queue (128 KB rows: 6.5 per SM
+//   33.1 against 34.8 us, 8 per SM 38.3 against 33.8 us);
+// - rows of 384 KB or more with K <= 31, any count: the row queue (500 KB rows at 50 per
+//   SM 541 against 569 us; the mixed workload's 594 KB rows 476 against 506 us; but
+//   250 KB rows at 16 per SM 104 against 98 us, and top-63 over 1 MB rows 3.60 against
+//   3.23 ms);
+// - otherwise warp ranges. LP_RAGGED_KERNEL=warp|queue forces one (a test hook).
+bool use_row_queue(uint32_t r_max, uint32_t V, uint32_t levels, int sms) {
+    const char* force = std::getenv("LP_RAGGED_KERNEL");
+    if (force && std::strcmp(force, "warp") == 0) return false;
+    if (force && std::strcmp(force, "queue") == 0) return true;
+    const uint64_t row_bytes = (uint64_t)V * 4u, per_sm = (uint64_t)sms;
+    if (r_max <= 3u * per_sm) return true;
+    if (row_bytes >= 60u * 1024u && r_max <= 7u * per_sm) return true;
+    return levels >= 1 && levels <= 5 && row_bytes >= 384u * 1024u;
+}
+
 bool device_info(int* dev_out, DeviceInfo** info) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
@@ -310,11 +332,8 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     int occ = occupancy(d, v, smem);
     if (occ == 0) return LP_ERR_CUDA;
     uint32_t grid = (uint32_t)d->sms * (uint32_t)occ;  // occ <= kMaxCtasPerSm
-    const char* force = std::getenv("LP_RAGGED_KERNEL");  // test hook: "warp" or "queue"
     const uint32_t r_max = T < T_logits ? T : T_logits;
-    bool queue = r_max <= 3u * (uint32_t)d->sms;
-    if (force && std::strcmp(force, "warp") == 0) queue = false;
-    if (force && std::strcmp(force, "queue") == 0) queue = true;
+    const bool queue = use_row_queue(r_max, V, levels, d->sms);
     size_t launch_smem = smem;
     unsigned block = lpk::kThreads;
     if (queue) {
@@ -484,6 +503,17 @@ lp_status lp_ragged_read_status(const void* workspace, uint32_t* host_status, lp
     if (cudaMemcpyAsync(host_status, &hdr->status, 4, cudaMemcpyDeviceToHost,
                         reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return LP_ERR_CUDA;
+    return LP_OK;
+}
+
+extern "C" lp_status lp_ragged_row_kernel(uint32_t T_logits, uint32_t T, uint32_t V, uint32_t levels,
+                                          int* kind) {
+    if (!kind) return LP_ERR_NULL;
+    if (levels > LP_MAX_LEVELS) return LP_ERR_LEVELS;
+    int dev;
+    DeviceInfo* d;
+    if (!device_info(&dev, &d)) return LP_ERR_CUDA;
+    *kind = use_row_queue(T < T_logits ? T : T_logits, V, levels, d->sms) ? 1 : 0;
     return LP_OK;
 }
 

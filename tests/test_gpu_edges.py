@@ -255,13 +255,22 @@ def test_split_vocab_pieces_echo_and_variants(split, monkeypatch):
     parity.check_batch(bv, what=f"variable+tau split={split}")
 
 
-@pytest.mark.parametrize("B,V", [(151, 20000), (152, 20000), (153, 20000), (304, 20000), (305, 20000),
-                                 (456, 20000), (457, 20000), (456, 70000), (457, 70000)])
-def test_kernel_choice_boundary(B, V):
-    # The library's own choice (152 SMs): split pieces below one row per SM, whole rows up
-    # to three per SM, then warp ranges.
-    b = workloads.make_next_token_batch(B, V, levels=3, dist="normal", scale=3.0, device="cuda", seed=B)
-    parity.check_batch(b, rows=parity.sample_rows(B, 40, seed=B), what=f"B={B} V={V}")
+@pytest.mark.parametrize("B,V,levels,per_sm", [
+    (151, 20000, 3, None), (152, 20000, 3, None), (153, 20000, 3, None), (304, 20000, 3, None),
+    (305, 20000, 3, None), (456, 8000, 3, 3), (457, 8000, 3, 3), (456, 70000, 3, 3), (457, 70000, 3, 3),
+    (1064, 16000, 3, 7), (1065, 16000, 3, 7), (1065, 100000, 3, 7), (1065, 100000, 6, 7)])
+def test_kernel_choice_boundary(B, V, levels, per_sm):
+    # The library's own choice: split pieces below one row per SM, whole rows up to three
+    # per SM; then the row queue up to seven rows per SM for rows of 60 KB or more, for any
+    # count of rows of 384 KB or more at K <= 31, else warp ranges. per_sm: the boundary
+    # the case sits at (on 152 SMs); the expected kernel follows the rule on this GPU.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    row_bytes = 4 * V
+    want = ("queue" if B <= 3 * sms or (row_bytes >= 60 * 1024 and B <= 7 * sms)
+            or (1 <= levels <= 5 and row_bytes >= 384 * 1024) else "warp")
+    assert lp.row_kernel(B, B, V, levels) == want
+    b = workloads.make_next_token_batch(B, V, levels=levels, dist="normal", scale=3.0, device="cuda", seed=B)
+    parity.check_batch(b, rows=parity.sample_rows(B, 40, seed=B), what=f"B={B} V={V} levels={levels} ({want})")
 
 
 @pytest.mark.parametrize("kernel", ["warp", "queue"])
