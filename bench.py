@@ -78,8 +78,8 @@ NCU_TRAFFIC = {
                       "lp_ragged_compute launches"},
     "prefill": {"source_hash": "f6565778a8e18f72", "kernel": "warp", "bytes_per_launch": 903528448,
                 "how": "--set full capture of one launch (its writes include lines the replay restored)"},
-    "mixed": {"source_hash": "f6565778a8e18f72", "kernel": "warp", "bytes_per_launch": 3348141893,
-              "how": "one-pass capture of a 12-batch sub-batch (1298 rows), scaled by rows to 5476"},
+    "mixed": {"source_hash": "f6565778a8e18f72", "kernel": "queue", "bytes_per_launch": 3345714026,
+              "how": "one-pass capture of a 12-batch sub-batch (1298 rows) on the row queue, scaled by rows to 5476"},
     "wide": {"source_hash": "f6565778a8e18f72", "kernel": "warp", "bytes_per_launch": 22188876239,
              "how": "one-pass capture of a 3-batch sub-batch (2670 rows), scaled by rows to 21598"},
 }
