@@ -73,14 +73,14 @@ def load_batch(config: str, variant: str, dev):
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the row kernel,
 # keyed by workload, valid only while the kernels' device code hashes to the recorded value.
 NCU_TRAFFIC = {
-    "decode": {"source_hash": "f6565778a8e18f72", "kernel": "queue", "bytes_per_launch": 131522304,
+    "decode": {"source_hash": "14c2f37baacc42df", "kernel": "queue", "bytes_per_launch": 131518976,
                "how": "one-pass launch list (dram__bytes_read.sum + dram__bytes_write.sum), median of the 100 "
                       "lp_ragged_compute launches"},
-    "prefill": {"source_hash": "f6565778a8e18f72", "kernel": "warp", "bytes_per_launch": 903528448,
+    "prefill": {"source_hash": "14c2f37baacc42df", "kernel": "warp", "bytes_per_launch": 903248640,
                 "how": "--set full capture of one launch (its writes include lines the replay restored)"},
-    "mixed": {"source_hash": "f6565778a8e18f72", "kernel": "queue", "bytes_per_launch": 3345714026,
+    "mixed": {"source_hash": "14c2f37baacc42df", "kernel": "queue", "bytes_per_launch": 3344303530,
               "how": "one-pass capture of a 12-batch sub-batch (1298 rows) on the row queue, scaled by rows to 5476"},
-    "wide": {"source_hash": "f6565778a8e18f72", "kernel": "warp", "bytes_per_launch": 22188876239,
+    "wide": {"source_hash": "14c2f37baacc42df", "kernel": "warp", "bytes_per_launch": 22186875828,
              "how": "one-pass capture of a 3-batch sub-batch (2670 rows), scaled by rows to 21598"},
 }
 

@@ -229,9 +229,12 @@ __device__ __forceinline__ uint64_t sk_owner(uint64_t v, uint64_t Q, uint64_t G)
 // Per-lane running sum in the log2 domain: s = sum of 2^(x*k - c) over the logits seen,
 // with a reference c that moves lazily. It is set by the first finite block and moved
 // up only when a block's maximum exceeds it by more than kHeadroom (so every term stays
-// below 2^kHeadroom and the sum far from overflow); any reference gives the same
-// logsumexp, c + log2(s). m, the lane's true running maximum, feeds the top-k bound.
-constexpr float kHeadroom = 8.f;
+// below 2^kHeadroom: a lane's sum of even 2^60 terms stays below the fp32 range); any
+// reference gives the same logsumexp, c + log2(s), with the same relative rounding. m,
+// the lane's true running maximum, feeds the top-k bound. A move costs a rescale and the
+// block's terms again; with 32 doublings of headroom it is rare even at small
+// temperatures (k = log2(e)/tau large).
+constexpr float kHeadroom = 32.f;
 constexpr float kNoRef = 3.402823466e38f;  // nc before the first finite logit
 struct LaneSum {
     float m;   // largest logit seen (-inf: none)
