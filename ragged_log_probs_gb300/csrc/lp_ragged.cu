@@ -323,10 +323,9 @@ static lp_status compute_impl(const float* logits, uint32_t T_logits, uint32_t V
     const size_t smem =
         kRingBytes + (p.stage_offsets ? (size_t)staged_arrays * (B + 1u) * sizeof(uint32_t) + ((B + 3u) & ~3u) : 0);
 
-    // Row queue when even all-echo input (R <= T, and R <= T_logits) gives at most three
-    // rows per SM; otherwise warp-owned ranges of the row space (the two kernels give the
-    // same result; the switch point comes from timing both on next-token shapes).
-    // Plain instantiation unless an extended input is given (it compiles without them).
+    // The row kernel by the bound R <= min(T, T_logits) and the row size (use_row_queue;
+    // the two kernels give the same result). Plain instantiation unless an extended input
+    // is given (it compiles without them).
     const bool ext = input_row_offsets != nullptr || temperatures != nullptr || tuples != nullptr;
     int v = variant_of(levels) + (ext ? kPerExt : 0);
     int occ = occupancy(d, v, smem);
